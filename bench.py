@@ -1,0 +1,390 @@
+"""Benchmark of the paged varlen relative-bias attention forward on GB300.
+
+One step = one rel_attn_paged_varlen call over the whole workload: the split
+heuristic, the main kernel and (when splits > 1) the LSE combine.  Inputs are
+seeded and synthetic (paged_attention_relative_gb300.workloads) and resident
+in HBM before timing; the KV cache (>= 512 MiB for the decode workloads) is
+larger than the 129 MB L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints one JSON line on rank 0.  Under torchrun every rank runs its own
+replica of the workload on its own GPU (the work shards by request and kv
+head with no exchange), so scaling is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode HBM TB/s & % roofline; prefill TFLOP/s & % bf16 peak (1×GB300)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DECODE = ("long_decode", "batched_decode", "tiny_mixed")
+KERNEL_SOURCES = {"decode": ["decode.cu", "common.cuh"], "prefill": ["prefill.cu", "common.cuh"]}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def kernel_hash(kind: str) -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kind]:
+        p = os.path.join(ROOT, "paged_attention_relative_gb300", "csrc", name)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kind: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_hash(kind)
+    for line in open(path):
+        parts = line.split("#")[0].split()
+        if len(parts) >= 4 and parts[0] == workload and parts[1] == kind and parts[2] == want:
+            return int(float(parts[3]))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+def make_workload(name: str):
+    from paged_attention_relative_gb300 import workloads as W
+    return W.WORKLOADS[name](0)
+
+
+def heuristic_splits(case, lib_splits):
+    d = case.dims
+    sk = case.cache_seqlens.tolist()
+    return lib_splits(case.window_left >= 0 or case.window_right >= 0, d["B"], max(case.seqlens_q), d["H"],
+                      d["Hk"], max(sk) if sk else 0)
+
+
+def run_ours(args, rank, world):
+    import torch
+
+    import paged_attention_relative_gb300 as pa
+    from paged_attention_relative_gb300 import _lib
+    from paged_attention_relative_gb300.roofline import algorithmic_bytes, algorithmic_flops
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    case = make_workload(args.workload)
+    if args.splits is not None:
+        splits = args.splits
+    elif args.workload == "long_decode":
+        splits = case.num_splits                  # the workload's own split count (16)
+    else:
+        splits = heuristic_splits(case, pa.rel_attn_num_splits)
+    g = {k: getattr(case, k).to(dev) for k in ("q", "key_cache", "value_cache", "block_table", "cache_seqlens",
+                                               "cu_seqlens_q", "rel_logits")}
+    out = torch.empty_like(g["q"])
+    stream = torch.cuda.current_stream(dev)
+
+    # Pre-built descriptors: the timed loop is the bare C-ABI call.
+    D = [_lib.describe(g[k]) for k in ("q", "key_cache", "value_cache", "block_table", "cache_seqlens",
+                                       "cu_seqlens_q")]
+    rel = _lib.describe(g["rel_logits"]) if case.rel_extent > 0 else None
+    od = _lib.describe(out)
+    import ctypes
+    refs = [ctypes.byref(d) for d in D]
+    rref = ctypes.byref(rel) if rel is not None else None
+    oref = ctypes.byref(od)
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    call_args = (*refs, case.max_seqlen_q, ctypes.c_float(case.softmax_scale), int(case.causal),
+                 case.window_left, case.window_right, case.rel_extent, rref, splits, oref, sptr)
+    fn = _lib.lib.rel_attn_paged_varlen
+
+    def step():
+        st = fn(*call_args)
+        if st != 0:
+            raise RuntimeError(_lib.lib.rel_attn_last_error().decode())
+
+    for _ in range(max(args.warmup, 1)):
+        step()
+    torch.cuda.synchronize()
+    info = pa.last_launch()
+    kind = info["kernel"]
+
+    barrier = (lambda: torch.distributed.barrier()) if world > 1 else (lambda: None)
+
+    # Whole-step timing.
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms_total = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+
+    # Main-kernel timing with events recorded by the library around the launch.
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for b, e in evs:
+        pa.set_kernel_events(b, e)
+        step()
+    pa.set_kernel_events(None, None)
+    torch.cuda.synchronize()
+    kern_ms = [b.elapsed_time(e) for b, e in evs]
+    kern_avg = sum(kern_ms) / len(kern_ms)
+
+    # End to end through the public API: pinned host inputs -> device, call,
+    # result -> pinned host, every step.  The paged KV cache stays resident.
+    host_in = {k: getattr(case, k).pin_memory() for k in ("q", "rel_logits", "block_table", "cache_seqlens",
+                                                           "cu_seqlens_q")}
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for k, v in host_in.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        pa.rel_attn_paged_varlen(dev_in["q"], g["key_cache"], g["value_cache"], dev_in["block_table"],
+                                 dev_in["cache_seqlens"], dev_in["cu_seqlens_q"], case.max_seqlen_q,
+                                 case.softmax_scale, case.causal, case.window_left, case.window_right,
+                                 case.rel_extent, dev_in["rel_logits"], splits, out=out)
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    a0 = torch.cuda.Event(enable_timing=True)
+    a1 = torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a0.elapsed_time(a1) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    nbytes = algorithmic_bytes(case)
+    flops = algorithmic_flops(case)
+    pk, pk_src = peaks()
+    decode = kind == "decode"
+    if decode:
+        value = world * nbytes / (ms_step * 1e-3) / 1e12
+        unit = "TB/s"
+        e2e_value = world * nbytes / (e2e_ms * 1e-3) / 1e12
+        ach = nbytes / (kern_avg * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / pk["hbm_gbs"], 4), "traffic": recorded_traffic(args.workload, kind),
+                "peak_source": f"{pk_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                if pk_src == "measured" else "fallback 6.8 TB/s",
+                "nominal_frac_8tbs": round(ach / 8000.0, 4)}
+    else:
+        value = world * flops / (ms_step * 1e-3) / 1e12
+        unit = "TFLOP/s"
+        e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+        ach = flops / (kern_avg * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(ach / pk["bf16_tflops"], 4), "traffic": recorded_traffic(args.workload, kind),
+                "peak_source": f"{pk_src} cuBLAS bf16 burst (MEASURED_PEAKS.json bf16_tflops)"}
+    d = case.dims
+    res = {
+        "metric": METRIC, "value": round(value, 4), "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, shuffled page pool)",
+        "config": {"workload": args.workload, "batch": d["B"], "tokens": d["T"], "num_heads": d["H"],
+                   "num_kv_heads": d["Hk"], "head_dim": d["D"], "block_size": d["BS"], "rel_extent": d["R"],
+                   "max_kv_len": int(case.cache_seqlens.max()), "num_splits": splits,
+                   "window": [case.window_left, case.window_right], "causal": case.causal,
+                   "parallelism": f"replicas{world}", "l2": "inputs larger than L2 (paged KV > 129 MB)",
+                   "algorithmic_bytes": nbytes, "algorithmic_flops": flops},
+        "kernel": {"name": kind, "avg_ms": round(kern_avg, 5), "launches_per_step": info["launches"],
+                   "grid": info["grid"], "block": info["block"], "smem_bytes": info["smem_bytes"]},
+        "roofline": roof,
+        "tokens_per_s": round(world * d["T"] / (ms_step * 1e-3), 1),
+        "e2e": {"value": round(e2e_value, 4), "unit": unit, "ms_per_step": round(e2e_ms, 5),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "pinned host q, rel_logits, block_table, cache_seqlens, cu_seqlens_q in; out back; paged KV resident"},
+        "gpu_launches": args.steps * info["launches"],
+        "clocks": clocks.summary(),
+    }
+    return res, case
+
+
+def time_oracle(case, budget_s: float):
+    """The fp64 oracle on the host cores, on a bounded sample of the workload's
+    output rows; returns (seconds per full workload, sample description, cores)."""
+    import numpy as np
+
+    from oracle import reference as ref
+    cores = ref.default_threads()
+    d = case.dims
+    T, H = d["T"], d["H"]
+    n_rows = T * H
+    rng = np.random.default_rng(0)
+    # Probe with a few rows, then size the sample to the budget.
+    probe = min(n_rows, max(cores, 8))
+    idx = rng.choice(n_rows, size=probe, replace=False)
+    t0 = time.perf_counter()
+    ref.forward_rows(case, idx // H, idx % H, num_threads=cores)
+    dt = time.perf_counter() - t0
+    per_row = dt / probe
+    n = int(min(n_rows, max(probe, budget_s / max(per_row, 1e-9))))
+    idx = rng.choice(n_rows, size=n, replace=False)
+    t0 = time.perf_counter()
+    ref.forward_rows(case, idx // H, idx % H, num_threads=cores)
+    dt = time.perf_counter() - t0
+    full = dt * n_rows / n
+    return full, f"{n} of {n_rows} (token, head) output rows chosen uniformly (seed 0), scaled to the whole workload", cores
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="long_decode")
+    ap.add_argument("--splits", type=int, default=None)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    res, case = run_ours(args, rank, world)
+    if rank == 0 and not args.no_cpu_baseline:
+        full_s, sample, cores = time_oracle(case, args.cpu_budget)
+        unit_work = res["config"]["algorithmic_bytes"] if res["unit"] == "TB/s" else res["config"]["algorithmic_flops"]
+        res["cpu_baseline"] = {"value": round(unit_work / full_s / 1e12, 6), "unit": res["unit"], "cores": cores,
+                               "kind": "oracle", "sample": sample, "seconds_per_step": round(full_s, 3)}
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, on the host cores, per step a bounded sample."""
+    if rank != 0:
+        return
+    from paged_attention_relative_gb300.roofline import algorithmic_bytes, algorithmic_flops
+    case = make_workload(args.workload)
+    decode = case.max_seqlen_q * (case.dims["H"] // case.dims["Hk"]) <= 64
+    work = algorithmic_bytes(case) if decode else algorithmic_flops(case)
+    unit = "TB/s" if decode else "TFLOP/s"
+    budget = max(1.0, 120.0 / max(args.steps + args.warmup, 1))
+    for _ in range(args.warmup):
+        time_oracle(case, min(budget, 2.0))
+    times = []
+    sample = cores = None
+    for _ in range(args.steps):
+        full_s, sample, cores = time_oracle(case, budget)
+        times.append(full_s)
+    s = statistics.mean(times)
+    value = work / s / 1e12
+    d = case.dims
+    res = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": unit, "n_gpus": 1,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s * 1e3, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) bf16)",
+           "config": {"workload": args.workload, "batch": d["B"], "tokens": d["T"], "num_heads": d["H"],
+                      "num_kv_heads": d["Hk"], "head_dim": d["D"], "rel_extent": d["R"]},
+           "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": cores, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,165 @@
+/*
+ * rel_attn.h - paged, variable-length attention with an additive
+ * relative-position bias (Inkling relative attention), for NVIDIA GB300
+ * (sm_103a).  Plain C ABI: borrowed tensor descriptors, a CUDA stream, a
+ * status code.  No exceptions, aborts or traps cross it.
+ *
+ * The operation follows the interface of inkling_fa4_rel_attention in the vLLM
+ * API docs for vllm.models.inkling.nvidia.ops.fa4_rel_attention (signature and
+ * docstring), with the bias rule of score_mod_rel_bias in the prhub report on
+ * vLLM PR #48858 ("关键源码片段", the source excerpt).  For request b with
+ * sq_b = cu_seqlens_q[b+1] - cu_seqlens_q[b] query tokens and
+ * sk_b = cache_seqlens[b] cached keys, query row i (global token
+ * t = cu_seqlens_q[b] + i) and query head h:
+ *
+ *   g      = h / (H / Hk)                                (GQA map)
+ *   K_j    = key_cache[block_table[b, j / BS], j % BS, g, :]   (V_j likewise)
+ *   d_j    = (i + sk_b - sq_b) - j                       (relative distance)
+ *   bias_j = rel_logits[t, h, d_j] if 0 <= d_j < rel_extent, else exactly 0
+ *   s_j    = softmax_scale * q[t,h,:] . K_j + bias_j     (bias after the scale)
+ *   allowed_j = j < sk_b  and (!causal || d_j >= 0)
+ *               and (window_left  < 0 || d_j <=  window_left)
+ *               and (window_right < 0 || d_j >= -window_right)
+ *   out[t,h,:] = sum_allowed softmax(s)_j V_j ;  0 if no key is allowed.
+ *
+ * The causal mask is aligned bottom-right (row i sits at key position
+ * i + sk_b - sq_b, the same offset the bias uses).
+ */
+#ifndef REL_ATTN_H
+#define REL_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* A cudaStream_t.  NULL is the legacy default stream. */
+typedef struct CUstream_st* rel_attn_stream;
+
+typedef enum {
+    REL_ATTN_BF16 = 0,
+    REL_ATTN_F32 = 1,
+    REL_ATTN_I32 = 2
+} rel_attn_dtype;
+
+/*
+ * Borrowed view of one tensor.  data is a DEVICE pointer; shape and stride
+ * are in elements (stride[k] is the element step of dimension k).  The
+ * library never keeps the pointer past the stream work of the call.
+ */
+typedef struct {
+    void* data;
+    int32_t dtype;      /* rel_attn_dtype */
+    int32_t ndim;
+    int64_t shape[4];
+    int64_t stride[4];
+} rel_attn_tensor;
+
+typedef enum {
+    REL_ATTN_OK = 0,
+    REL_ATTN_ERR_INVALID_ARGUMENT = 1,
+    REL_ATTN_ERR_UNSUPPORTED = 2,
+    REL_ATTN_ERR_CUDA = 3,
+    REL_ATTN_ERR_OUT_OF_MEMORY = 4,
+    REL_ATTN_ERR_DEVICE_CHECK = 5
+} rel_attn_status;
+
+/*
+ * rel_attn_paged_varlen - the forward.  Defined by inkling_fa4_rel_attention
+ * (vLLM API docs, fa4_rel_attention); bias rule from score_mod_rel_bias (prhub
+ * report on PR #48858, source excerpt).
+ *
+ * Arguments (all tensors on the current CUDA device, sm_103):
+ *   q              (T, H, D) bf16; last dim contiguous, strides 16-byte multiples
+ *   key_cache      (NB, BS, Hk, D) bf16; last dim contiguous; base 16-byte aligned,
+ *                  other strides 16-byte multiples (read by TMA)
+ *   value_cache    same shape and layout rules as key_cache
+ *   block_table    (B, MB) int32, row-major contiguous: physical block of
+ *                  request b's logical block n
+ *   cache_seqlens  (B,) int32 = seqused_k, 0 <= sk_b <= MB * BS
+ *   cu_seqlens_q   (B+1,) int32, cu[0] = 0, non-decreasing, cu[B] = T
+ *   max_seqlen_q   >= every sq_b (the kernel choice and grid come from it)
+ *   softmax_scale  multiplies q.k before the bias is added
+ *   causal         nonzero: bottom-right aligned causal mask
+ *   window_left, window_right
+ *                  sliding window in keys; a negative side is unbounded;
+ *                  (-1, -1) means no window
+ *   rel_extent     R >= 0; R == 0 means no bias (rel_logits may then be NULL)
+ *   rel_logits     (T, H, R) bf16, fully contiguous (the pages make the bias
+ *                  tensor contiguous before the call)
+ *   num_splits     >= 1: a cap on the number of KV splits per (request, kv head);
+ *                  1 writes out directly, >1 writes fp32 partials and runs an
+ *                  LSE-weighted combine.  Clamped to what the KV length allows.
+ *   out            (T, H, D) bf16 (or fp32, which keeps the result before the
+ *                  final bf16 rounding), caller-allocated; must not alias an input
+ *   stream         the stream all work is ordered on
+ *
+ * Supported: D in {64, 128}; BS a multiple of 16; H % Hk == 0; H / Hk <= 128.
+ *
+ * Ownership: every tensor is caller-owned device memory, borrowed until the
+ * stream work completes.  When num_splits > 1 the library allocates a
+ * stream-ordered workspace (cudaMallocAsync / cudaFreeAsync on `stream`) of
+ * num_splits * T * H * (D + 1) * 4 bytes.
+ *
+ * Errors: REL_ATTN_ERR_INVALID_ARGUMENT for a NULL pointer with a nonzero
+ * size, a dtype/rank/shape/stride mismatch, H % Hk != 0, num_splits < 1 or
+ * rel_extent < 0; REL_ATTN_ERR_UNSUPPORTED for another D or BS, a device that
+ * is not sm_103, or a layout TMA cannot address; REL_ATTN_ERR_OUT_OF_MEMORY
+ * when the workspace cannot be allocated; REL_ATTN_ERR_CUDA for a launch
+ * error.  rel_attn_last_error() then describes it.  T == 0 returns OK and
+ * launches nothing.  Device-side preconditions (monotone cu_seqlens_q,
+ * sq_b <= max_seqlen_q, block ids < NB, sk_b <= MB * BS) are documented, not
+ * checked, unless the environment variable REL_ATTN_CHECK=1 is set, in which
+ * case a check kernel runs first, the call synchronises `stream`, and a
+ * violation returns REL_ATTN_ERR_DEVICE_CHECK without running the forward.
+ */
+rel_attn_status rel_attn_paged_varlen(
+    const rel_attn_tensor* q,
+    const rel_attn_tensor* key_cache,
+    const rel_attn_tensor* value_cache,
+    const rel_attn_tensor* block_table,
+    const rel_attn_tensor* cache_seqlens,
+    const rel_attn_tensor* cu_seqlens_q,
+    int32_t max_seqlen_q,
+    float softmax_scale,
+    int32_t causal,
+    int32_t window_left,
+    int32_t window_right,
+    int32_t rel_extent,
+    const rel_attn_tensor* rel_logits,
+    int32_t num_splits,
+    rel_attn_tensor* out,
+    rel_attn_stream stream);
+
+/*
+ * rel_attn_num_splits - split-KV cap for this attention, defined by
+ * inkling_fa4_num_splits (vLLM API docs, fa4_rel_attention) without its
+ * Hopper branch (this library runs on sm_103 only).  Local (windowed)
+ * attention gets 1.  Otherwise the GQA-packed query rows
+ * max_query_len * (num_heads / num_kv_heads) are cut into 256-row tiles,
+ * base = batch_size * num_kv_heads * tiles, target = 256 (one tile, batch 1),
+ * 128 (one tile) or 64, a batch-1 single-tile cap of 16 (8 kv heads), 32
+ * (4 kv heads or KV <= 8192), 64 (KV <= 65536) or 128, else a cap of 128;
+ * the result is max(1, min(target / base, cap, ceil(max_kv_len / 128))).
+ * Pure host integer logic; no device is touched.
+ * Returns >= 1, or -REL_ATTN_ERR_INVALID_ARGUMENT when batch_size < 1,
+ * max_query_len < 1, num_heads < 1, num_kv_heads < 1,
+ * num_heads % num_kv_heads != 0 or max_kv_len < 0.
+ */
+int32_t rel_attn_num_splits(int32_t is_local, int32_t batch_size, int32_t max_query_len,
+                            int32_t num_heads, int32_t num_kv_heads, int32_t max_kv_len);
+
+/*
+ * rel_attn_last_error - thread-local, NUL-terminated description of the last
+ * non-OK status returned on this thread ("" if none).  Owned by the library;
+ * valid until the next call on the same thread.
+ */
+const char* rel_attn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* REL_ATTN_H */

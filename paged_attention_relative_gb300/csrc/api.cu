@@ -1,0 +1,445 @@
+// C ABI of the library: argument validation, TMA descriptors, kernel choice,
+// stream-ordered split workspace, launch.  Declared in include/rel_attn.h and
+// include/rel_attn_profile.h.
+//
+// The interface follows inkling_fa4_rel_attention and inkling_fa4_num_splits
+// in the vLLM API docs for vllm.models.inkling.nvidia.ops.fa4_rel_attention.
+
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "kernels.h"
+#include "rel_attn.h"
+#include "rel_attn_profile.h"
+
+namespace relattn {
+
+__device__ int g_device_error = 0;
+__device__ int g_check_error = 0;
+
+namespace {
+
+thread_local std::string t_last_error;
+thread_local rel_attn_launch_info t_launch = {};
+thread_local cudaEvent_t t_ev_begin = nullptr;
+thread_local cudaEvent_t t_ev_end = nullptr;
+
+rel_attn_status fail(rel_attn_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+rel_attn_status fail(rel_attn_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return st;
+}
+
+struct DeviceInfo {
+    bool ready = false;
+    int major = 0, minor = 0, sms = 0;
+    int* err = nullptr;
+    int* check_err = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+rel_attn_status device_info(DeviceInfo** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(REL_ATTN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(REL_ATTN_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        cudaDeviceProp prop;
+        e = cudaGetDeviceProperties(&prop, dev);
+        if (e != cudaSuccess) return fail(REL_ATTN_ERR_CUDA, "cudaGetDeviceProperties: %s", cudaGetErrorString(e));
+        d.major = prop.major;
+        d.minor = prop.minor;
+        d.sms = prop.multiProcessorCount;
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_device_error);
+        if (e != cudaSuccess) return fail(REL_ATTN_ERR_CUDA, "error word: %s", cudaGetErrorString(e));
+        d.err = static_cast<int*>(p);
+        e = cudaGetSymbolAddress(&p, g_check_error);
+        if (e != cudaSuccess) return fail(REL_ATTN_ERR_CUDA, "check word: %s", cudaGetErrorString(e));
+        d.check_err = static_cast<int*>(p);
+        d.ready = true;
+    }
+    *out = &d;
+    return REL_ATTN_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Paged cache (NB, BS, Hk, D) as a 4-D TMA tensor, innermost first:
+// (D, Hk, BS, NB), box (64 dims, 1 head, 16 slots, 1 block), 128-byte swizzle.
+rel_attn_status make_cache_map(const rel_attn_tensor* t, CUtensorMap* map, const char* name) {
+    auto enc = encode_fn();
+    if (!enc) return fail(REL_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[4] = {(cuuint64_t)t->shape[3], (cuuint64_t)t->shape[2], (cuuint64_t)t->shape[1],
+                          (cuuint64_t)t->shape[0]};
+    cuuint64_t strides[3] = {(cuuint64_t)t->stride[2] * 2, (cuuint64_t)t->stride[1] * 2,
+                             (cuuint64_t)t->stride[0] * 2};
+    cuuint32_t box[4] = {64, 1, 16, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t->data, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(REL_ATTN_ERR_UNSUPPORTED, "%s: TMA descriptor rejected (CUresult %d)", name, (int)r);
+    return REL_ATTN_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+rel_attn_status check_tensor(const rel_attn_tensor* t, const char* name, int dtype, int ndim) {
+    if (!t) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "%s: descriptor is NULL", name);
+    if (t->dtype != dtype) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "%s: dtype %d, expected %d", name, t->dtype, dtype);
+    if (t->ndim != ndim) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "%s: rank %d, expected %d", name, t->ndim, ndim);
+    int64_t n = 1;
+    for (int i = 0; i < ndim; ++i) {
+        if (t->shape[i] < 0) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "%s: negative extent", name);
+        n *= t->shape[i];
+    }
+    if (n > 0 && !t->data) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "%s: NULL data with %lld elements", name, (long long)n);
+    return REL_ATTN_OK;
+}
+
+int64_t span_bytes(const rel_attn_tensor* t, int elem) {
+    int64_t last = 0;
+    for (int i = 0; i < t->ndim; ++i) {
+        if (t->shape[i] == 0) return 0;
+        last += (t->shape[i] - 1) * t->stride[i];
+    }
+    return (last + 1) * elem;
+}
+
+bool overlaps(const rel_attn_tensor* a, int ea, const rel_attn_tensor* b, int eb) {
+    if (!a || !b || !a->data || !b->data) return false;
+    const int64_t na = span_bytes(a, ea), nb = span_bytes(b, eb);
+    if (na == 0 || nb == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a->data), b0 = reinterpret_cast<uintptr_t>(b->data);
+    return a0 < b0 + (uintptr_t)nb && b0 < a0 + (uintptr_t)na;
+}
+
+uint64_t wait_timeout_ns() {
+    static uint64_t ns = [] {
+        const char* s = std::getenv("REL_ATTN_WAIT_TIMEOUT_MS");
+        long long ms = s ? std::atoll(s) : 0;
+        if (ms <= 0) ms = 2000;
+        return (uint64_t)ms * 1000000ull;
+    }();
+    return ns;
+}
+
+bool check_enabled() {
+    const char* s = std::getenv("REL_ATTN_CHECK");
+    return s && s[0] == '1';
+}
+
+// Device-side precondition check (REL_ATTN_CHECK=1): one thread per request.
+__global__ void check_kernel(const int32_t* cu, const int32_t* seqk, const int32_t* table, int64_t bt_stride, int B,
+                             int T, int MB, int BS, int NB, int max_seqlen_q, int* err) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    int code = 0;
+    const int sq = cu[b + 1] - cu[b];
+    if (b == 0 && cu[0] != 0) code = 1;
+    if (b == B - 1 && cu[B] != T) code = 2;
+    if (sq < 0) code = 3;
+    if (sq > max_seqlen_q) code = 4;
+    const int sk = seqk[b];
+    if (sk < 0 || (long long)sk > (long long)MB * BS) code = 5;
+    if (!code) {
+        const int nblk = (sk + BS - 1) / BS;
+        for (int n = 0; n < nblk; ++n) {
+            const int blk = table[(size_t)b * bt_stride + n];
+            if (blk < 0 || blk >= NB) {
+                code = 6;
+                break;
+            }
+        }
+    }
+    if (code) atomicCAS(err, 0, code);
+}
+
+}  // namespace
+}  // namespace relattn
+
+using namespace relattn;
+
+extern "C" const char* rel_attn_last_error(void) { return t_last_error.c_str(); }
+
+extern "C" int32_t rel_attn_num_splits(int32_t is_local, int32_t batch_size, int32_t max_query_len,
+                                       int32_t num_heads, int32_t num_kv_heads, int32_t max_kv_len) {
+    if (batch_size < 1 || max_query_len < 1 || num_heads < 1 || num_kv_heads < 1 || num_heads % num_kv_heads != 0 ||
+        max_kv_len < 0) {
+        fail(REL_ATTN_ERR_INVALID_ARGUMENT, "rel_attn_num_splits: invalid sizes");
+        return -REL_ATTN_ERR_INVALID_ARGUMENT;
+    }
+    if (is_local) return 1;
+    const int64_t rows = (int64_t)max_query_len * (num_heads / num_kv_heads);
+    const int64_t tiles = (rows + 255) / 256;
+    const int64_t base = (int64_t)batch_size * num_kv_heads * tiles;
+    const bool one_tile_b1 = tiles == 1 && batch_size == 1;
+    const int64_t target = one_tile_b1 ? 256 : (tiles == 1 ? 128 : 64);
+    int64_t cap = 128;
+    if (one_tile_b1) {
+        if (num_kv_heads == 8)
+            cap = 16;
+        else if (num_kv_heads == 4 || max_kv_len <= 8192)
+            cap = 32;
+        else if (max_kv_len <= 65536)
+            cap = 64;
+        else
+            cap = 128;
+    }
+    const int64_t kv_blocks = ((int64_t)max_kv_len + 127) / 128;
+    int64_t r = target / base;
+    if (cap < r) r = cap;
+    if (kv_blocks < r) r = kv_blocks;
+    return (int32_t)(r < 1 ? 1 : r);
+}
+
+extern "C" rel_attn_status rel_attn_last_launch(rel_attn_launch_info* info) {
+    if (!info) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "info is NULL");
+    *info = t_launch;
+    return REL_ATTN_OK;
+}
+
+extern "C" rel_attn_status rel_attn_set_kernel_events(void* begin, void* end) {
+    if ((begin == nullptr) != (end == nullptr))
+        return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "pass both events or neither");
+    t_ev_begin = static_cast<cudaEvent_t>(begin);
+    t_ev_end = static_cast<cudaEvent_t>(end);
+    return REL_ATTN_OK;
+}
+
+extern "C" rel_attn_status rel_attn_device_error(int32_t* code) {
+    if (!code) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "code is NULL");
+    DeviceInfo* dev = nullptr;
+    rel_attn_status st = device_info(&dev);
+    if (st != REL_ATTN_OK) return st;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail(REL_ATTN_ERR_CUDA, "cudaDeviceSynchronize: %s", cudaGetErrorString(e));
+    int v = 0;
+    e = cudaMemcpy(&v, dev->err, sizeof v, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(dev->err, 0, sizeof v);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail(REL_ATTN_ERR_CUDA, "reading the error word: %s", cudaGetErrorString(e));
+    *code = v;
+    return REL_ATTN_OK;
+}
+
+extern "C" rel_attn_status rel_attn_paged_varlen(
+    const rel_attn_tensor* q, const rel_attn_tensor* key_cache, const rel_attn_tensor* value_cache,
+    const rel_attn_tensor* block_table, const rel_attn_tensor* cache_seqlens, const rel_attn_tensor* cu_seqlens_q,
+    int32_t max_seqlen_q, float softmax_scale, int32_t causal, int32_t window_left, int32_t window_right,
+    int32_t rel_extent, const rel_attn_tensor* rel_logits, int32_t num_splits, rel_attn_tensor* out,
+    rel_attn_stream stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    t_launch = rel_attn_launch_info{};
+    rel_attn_status st;
+    if ((st = check_tensor(q, "q", REL_ATTN_BF16, 3))) return st;
+    if ((st = check_tensor(key_cache, "key_cache", REL_ATTN_BF16, 4))) return st;
+    if ((st = check_tensor(value_cache, "value_cache", REL_ATTN_BF16, 4))) return st;
+    if ((st = check_tensor(block_table, "block_table", REL_ATTN_I32, 2))) return st;
+    if ((st = check_tensor(cache_seqlens, "cache_seqlens", REL_ATTN_I32, 1))) return st;
+    if ((st = check_tensor(cu_seqlens_q, "cu_seqlens_q", REL_ATTN_I32, 1))) return st;
+    if (!out) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "out: descriptor is NULL");
+    if ((st = check_tensor(out, "out", out->dtype == REL_ATTN_F32 ? REL_ATTN_F32 : REL_ATTN_BF16, 3))) return st;
+    const int out_elem = out->dtype == REL_ATTN_F32 ? 4 : 2;
+
+    const int64_t T = q->shape[0], H = q->shape[1], D = q->shape[2];
+    const int64_t NB = key_cache->shape[0], BS = key_cache->shape[1], Hk = key_cache->shape[2];
+    const int64_t B = block_table->shape[0], MB = block_table->shape[1];
+    for (int i = 0; i < 4; ++i)
+        if (value_cache->shape[i] != key_cache->shape[i])
+            return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "value_cache shape differs from key_cache");
+    if (key_cache->shape[3] != D) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "cache head_dim %lld != q head_dim %lld",
+                                              (long long)key_cache->shape[3], (long long)D);
+    if (out->shape[0] != T || out->shape[1] != H || out->shape[2] != D)
+        return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "out shape must equal q shape");
+    if (cache_seqlens->shape[0] != B) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "cache_seqlens must have B entries");
+    if (cu_seqlens_q->shape[0] != B + 1) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "cu_seqlens_q must have B+1 entries");
+    if (cache_seqlens->stride[0] != 1 || cu_seqlens_q->stride[0] != 1)
+        return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "cache_seqlens and cu_seqlens_q must be contiguous");
+    if (MB > 0 && block_table->stride[1] != 1)
+        return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "block_table rows must be contiguous");
+    if (B > 0 && block_table->stride[0] < MB)
+        return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "block_table row stride smaller than its width");
+    if (H <= 0 || Hk <= 0 || H % Hk != 0)
+        return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "num_heads %lld must be a positive multiple of num_kv_heads %lld",
+                    (long long)H, (long long)Hk);
+    if (num_splits < 1) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "num_splits must be >= 1 (got %d)", num_splits);
+    if (rel_extent < 0) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "rel_extent must be >= 0 (got %d)", rel_extent);
+    if (max_seqlen_q < 0) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "max_seqlen_q must be >= 0");
+    if (rel_extent > 0) {
+        if ((st = check_tensor(rel_logits, "rel_logits", REL_ATTN_BF16, 3))) return st;
+        if (rel_logits->shape[0] != T || rel_logits->shape[1] != H || rel_logits->shape[2] != rel_extent)
+            return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "rel_logits must be (T, H, rel_extent)");
+        if (rel_logits->stride[2] != 1 || rel_logits->stride[1] != rel_extent ||
+            rel_logits->stride[0] != H * rel_extent)
+            return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "rel_logits must be contiguous");
+    }
+    if (q->stride[2] != 1 || out->stride[2] != 1 || key_cache->stride[3] != 1 || value_cache->stride[3] != 1)
+        return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "the head_dim axis must be contiguous");
+    if (D != 64 && D != 128) return fail(REL_ATTN_ERR_UNSUPPORTED, "head_dim %lld unsupported (64 or 128)", (long long)D);
+    if (BS <= 0 || BS % 16 != 0)
+        return fail(REL_ATTN_ERR_UNSUPPORTED, "block_size %lld unsupported (a multiple of 16)", (long long)BS);
+    if (H / Hk > 128) return fail(REL_ATTN_ERR_UNSUPPORTED, "more than 128 query heads per kv head");
+    if (T > INT32_MAX / 2 || NB > INT32_MAX || H * T > ((int64_t)1 << 40))
+        return fail(REL_ATTN_ERR_UNSUPPORTED, "sizes beyond 32-bit indexing");
+    if (T > 0 && max_seqlen_q < 1) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "max_seqlen_q must be >= 1 when T > 0");
+    if (overlaps(out, out_elem, q, 2) || overlaps(out, out_elem, key_cache, 2) ||
+        overlaps(out, out_elem, value_cache, 2) || (rel_extent > 0 && overlaps(out, out_elem, rel_logits, 2)))
+        return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "out aliases an input");
+    if (T == 0 || B == 0) {
+        t_launch.kernel = REL_ATTN_KERNEL_NONE;
+        return REL_ATTN_OK;
+    }
+    // Alignment rules of the vector loads and TMA.
+    const int64_t oal = 16 / out_elem;
+    if (!aligned(q->data, 16) || q->stride[0] % 8 || q->stride[1] % 8 || !aligned(out->data, 16) ||
+        out->stride[0] % oal || out->stride[1] % oal)
+        return fail(REL_ATTN_ERR_UNSUPPORTED, "q/out need 16-byte aligned bases and strides");
+    for (const rel_attn_tensor* c : {key_cache, value_cache})
+        if (!aligned(c->data, 16) || c->stride[0] % 8 || c->stride[1] % 8 || c->stride[2] % 8)
+            return fail(REL_ATTN_ERR_UNSUPPORTED, "caches need 16-byte aligned bases and strides");
+
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev))) return st;
+    if (dev->major != 10 || dev->minor != 3)
+        return fail(REL_ATTN_ERR_UNSUPPORTED, "built for sm_103a; device is sm_%d%d", dev->major, dev->minor);
+
+    const int64_t G = H / Hk;
+    const int64_t rows = (int64_t)max_seqlen_q * G;
+    if (rows > 64)
+        return fail(REL_ATTN_ERR_UNSUPPORTED, "max_seqlen_q * (H / Hk) = %lld > 64 needs the prefill kernel",
+                    (long long)rows);
+
+    if (check_enabled()) {
+        cudaError_t e = cudaMemsetAsync(dev->check_err, 0, sizeof(int), stream);
+        if (e == cudaSuccess) {
+            check_kernel<<<(unsigned)((B + 127) / 128), 128, 0, stream>>>(
+                static_cast<const int32_t*>(cu_seqlens_q->data), static_cast<const int32_t*>(cache_seqlens->data),
+                static_cast<const int32_t*>(block_table->data), block_table->stride[0], (int)B, (int)T, (int)MB,
+                (int)BS, (int)NB, max_seqlen_q, dev->check_err);
+            e = cudaGetLastError();
+        }
+        int code = 0;
+        if (e == cudaSuccess) e = cudaMemcpyAsync(&code, dev->check_err, sizeof code, cudaMemcpyDeviceToHost, stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+        if (e != cudaSuccess) return fail(REL_ATTN_ERR_CUDA, "check kernel: %s", cudaGetErrorString(e));
+        if (code)
+            return fail(REL_ATTN_ERR_DEVICE_CHECK, "device-side precondition violated (code %d: %s)", code,
+                        code == 1 ? "cu_seqlens_q[0] != 0" : code == 2 ? "cu_seqlens_q[B] != T"
+                        : code == 3 ? "cu_seqlens_q decreasing" : code == 4 ? "a query length exceeds max_seqlen_q"
+                        : code == 5 ? "cache_seqlens outside [0, MB*BS]" : "block id outside [0, NB)");
+    }
+
+    CUtensorMap tmK, tmV;
+    if ((st = make_cache_map(key_cache, &tmK, "key_cache"))) return st;
+    if ((st = make_cache_map(value_cache, &tmV, "value_cache"))) return st;
+
+    AttnParams p{};
+    p.q = q->data;
+    p.q_st = q->stride[0];
+    p.q_sh = q->stride[1];
+    p.block_table = static_cast<const int32_t*>(block_table->data);
+    p.bt_stride = block_table->stride[0];
+    p.max_blocks = (int32_t)MB;
+    p.cache_seqlens = static_cast<const int32_t*>(cache_seqlens->data);
+    p.cu_seqlens_q = static_cast<const int32_t*>(cu_seqlens_q->data);
+    p.rel = rel_extent > 0 ? rel_logits->data : nullptr;
+    p.R = rel_extent;
+    p.out = out->data;
+    p.o_st = out->stride[0];
+    p.o_sh = out->stride[1];
+    p.out_f32 = out->dtype == REL_ATTN_F32 ? 1 : 0;
+    p.B = (int32_t)B;
+    p.T = (int32_t)T;
+    p.H = (int32_t)H;
+    p.Hk = (int32_t)Hk;
+    p.G = (int32_t)G;
+    p.BS = (int32_t)BS;
+    p.D = (int32_t)D;
+    p.max_rows = (int32_t)rows;
+    p.max_seqlen_q = max_seqlen_q;
+    p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.causal = causal ? 1 : 0;
+    p.wl = window_left;
+    p.wr = window_right;
+    p.timeout_ns = wait_timeout_ns();
+    p.err = dev->err;
+
+    // Splits: a cap, clamped to the 16-key slices a request can have.
+    int64_t max_keys = MB * BS;
+    int64_t splits = num_splits;
+    const int64_t slice_cap = (max_keys + 15) / 16;
+    if (splits > slice_cap) splits = slice_cap < 1 ? 1 : slice_cap;
+    if (splits > 1024) splits = 1024;
+    p.num_splits = (int32_t)splits;
+
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+    if (splits > 1) {
+        ws_bytes = (size_t)splits * T * H * (D + 1) * sizeof(float);
+        cudaError_t e = cudaMallocAsync(&ws, ws_bytes, stream);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(e == cudaErrorMemoryAllocation ? REL_ATTN_ERR_OUT_OF_MEMORY : REL_ATTN_ERR_CUDA,
+                        "split workspace of %zu bytes: %s", ws_bytes, cudaGetErrorString(e));
+        }
+        p.ws_o = static_cast<float*>(ws);
+        p.ws_lse = p.ws_o + (size_t)splits * T * H * D;
+    }
+
+    LaunchShape shape = decode_shape(p, dev->sms);
+    p.nstage = shape.nstage;
+    if (t_ev_begin) cudaEventRecord(t_ev_begin, stream);
+    cudaError_t e = launch_decode(p, tmK, tmV, shape, stream);
+    if (t_ev_end) cudaEventRecord(t_ev_end, stream);
+    int launches = 1;
+    if (e == cudaSuccess && splits > 1) {
+        e = launch_combine(p, stream);
+        ++launches;
+    }
+    if (ws) {
+        cudaError_t e2 = cudaFreeAsync(ws, stream);
+        if (e == cudaSuccess) e = e2;
+    }
+    t_launch.kernel = REL_ATTN_KERNEL_DECODE;
+    t_launch.num_splits = (int32_t)splits;
+    t_launch.grid[0] = (int32_t)shape.grid.x;
+    t_launch.grid[1] = (int32_t)shape.grid.y;
+    t_launch.grid[2] = (int32_t)shape.grid.z;
+    t_launch.block = shape.block;
+    t_launch.smem_bytes = shape.smem;
+    t_launch.launches = launches;
+    t_launch.workspace_bytes = (int64_t)ws_bytes;
+    if (e != cudaSuccess) return fail(REL_ATTN_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+    return REL_ATTN_OK;
+}

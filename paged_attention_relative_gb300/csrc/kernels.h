@@ -1,0 +1,52 @@
+// Host-side launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace relattn {
+
+// Everything a kernel needs besides the tensor maps.  Strides in elements.
+struct AttnParams {
+    const void* q;             // (T, H, D) bf16
+    int64_t q_st, q_sh;        // token / head strides
+    const int32_t* block_table;
+    int64_t bt_stride;         // MB
+    int32_t max_blocks;        // MB
+    const int32_t* cache_seqlens;
+    const int32_t* cu_seqlens_q;
+    const void* rel;           // (T, H, R) bf16 contiguous, or null when R == 0
+    int32_t R;
+    void* out;                 // (T, H, D) bf16, or fp32 when out_f32
+    int64_t o_st, o_sh;
+    int32_t out_f32;
+    float* ws_o;               // (S, T, H, D) fp32 partials when num_splits > 1
+    float* ws_lse;             // (S, T, H) fp32 log2-sum-exp partials
+    int32_t B, T, H, Hk, G, BS, D;
+    int32_t num_splits;
+    int32_t max_rows;          // max_seqlen_q * G (decode: <= 64)
+    int32_t max_seqlen_q;
+    float scale_log2;          // softmax_scale * log2(e)
+    int32_t causal, wl, wr;
+    int32_t nstage;
+    uint64_t timeout_ns;
+    int* err;                  // device error word (bounded-wait timeouts)
+};
+
+struct LaunchShape {
+    dim3 grid;
+    int block = 0;
+    int smem = 0;
+    int nstage = 0;
+};
+
+// Split-KV decode kernel for <= 64 GQA-packed rows per (request, kv head).
+LaunchShape decode_shape(const AttnParams& p, int num_sms);
+cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                          const LaunchShape& shape, cudaStream_t stream);
+
+// LSE-weighted merge of split partials into bf16 out.
+cudaError_t launch_combine(const AttnParams& p, cudaStream_t stream);
+
+}  // namespace relattn
