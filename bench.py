@@ -202,6 +202,9 @@ def run_ours(args, rank, world):
 
     # Main-kernel timing with events recorded by the library around the launch.
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for b, e in evs:          # torch creates the CUDA event on first record
+        b.record(stream)
+        e.record(stream)
     for b, e in evs:
         pa.set_kernel_events(b, e)
         step()

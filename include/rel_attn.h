@@ -74,8 +74,8 @@ typedef enum {
  * Arguments (all tensors on the current CUDA device, sm_103):
  *   q              (T, H, D) bf16; last dim contiguous, strides 16-byte multiples
  *   key_cache      (NB, BS, Hk, D) bf16; last dim contiguous; base 16-byte aligned,
- *                  other strides 16-byte multiples (read by TMA)
- *   value_cache    same shape and layout rules as key_cache
+ *                  other strides 16-byte multiples
+ *   value_cache    same shape and strides as key_cache
  *   block_table    (B, MB) int32, row-major contiguous: physical block of
  *                  request b's logical block n
  *   cache_seqlens  (B,) int32 = seqused_k, 0 <= sk_b <= MB * BS

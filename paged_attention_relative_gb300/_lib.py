@@ -136,7 +136,10 @@ def last_launch() -> dict:
 
 
 def set_kernel_events(begin: torch.cuda.Event | None, end: torch.cuda.Event | None):
-    """Record ``begin``/``end`` around the main kernel of following calls."""
+    """Record ``begin``/``end`` around the main kernel of following calls.
+
+    torch creates an event's CUDA handle lazily: record each event once before
+    passing it here."""
     b = ctypes.c_void_p(begin.cuda_event) if begin is not None else None
     e = ctypes.c_void_p(end.cuda_event) if end is not None else None
     _check(lib.rel_attn_set_kernel_events(b, e))

@@ -96,7 +96,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // Paged cache (NB, BS, Hk, D) as a 4-D TMA tensor, innermost first:
 // (D, Hk, BS, NB), box (64 dims, 1 head, 16 slots, 1 block), 128-byte swizzle.
-rel_attn_status make_cache_map(const rel_attn_tensor* t, CUtensorMap* map, const char* name) {
+[[maybe_unused]] rel_attn_status make_cache_map(const rel_attn_tensor* t, CUtensorMap* map, const char* name) {
     auto enc = encode_fn();
     if (!enc) return fail(REL_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t dims[4] = {(cuuint64_t)t->shape[3], (cuuint64_t)t->shape[2], (cuuint64_t)t->shape[1],
@@ -278,6 +278,9 @@ extern "C" rel_attn_status rel_attn_paged_varlen(
     for (int i = 0; i < 4; ++i)
         if (value_cache->shape[i] != key_cache->shape[i])
             return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "value_cache shape differs from key_cache");
+    for (int i = 0; i < 4; ++i)
+        if (value_cache->stride[i] != key_cache->stride[i])
+            return fail(REL_ATTN_ERR_UNSUPPORTED, "value_cache strides must equal key_cache strides");
     if (key_cache->shape[3] != D) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "cache head_dim %lld != q head_dim %lld",
                                               (long long)key_cache->shape[3], (long long)D);
     if (out->shape[0] != T || out->shape[1] != H || out->shape[2] != D)
@@ -360,14 +363,16 @@ extern "C" rel_attn_status rel_attn_paged_varlen(
                         : code == 5 ? "cache_seqlens outside [0, MB*BS]" : "block id outside [0, NB)");
     }
 
-    CUtensorMap tmK, tmV;
-    if ((st = make_cache_map(key_cache, &tmK, "key_cache"))) return st;
-    if ((st = make_cache_map(value_cache, &tmV, "value_cache"))) return st;
-
     AttnParams p{};
     p.q = q->data;
     p.q_st = q->stride[0];
     p.q_sh = q->stride[1];
+    p.k_cache = key_cache->data;
+    p.v_cache = value_cache->data;
+    p.c_s0 = key_cache->stride[0];
+    p.c_s1 = key_cache->stride[1];
+    p.c_s2 = key_cache->stride[2];
+    p.NB = (int32_t)NB;
     p.block_table = static_cast<const int32_t*>(block_table->data);
     p.bt_stride = block_table->stride[0];
     p.max_blocks = (int32_t)MB;
@@ -419,8 +424,9 @@ extern "C" rel_attn_status rel_attn_paged_varlen(
 
     LaunchShape shape = decode_shape(p, dev->sms);
     p.nstage = shape.nstage;
+    p.nprod = shape.nprod;
     if (t_ev_begin) cudaEventRecord(t_ev_begin, stream);
-    cudaError_t e = launch_decode(p, tmK, tmV, shape, stream);
+    cudaError_t e = launch_decode(p, shape, stream);
     if (t_ev_end) cudaEventRecord(t_ev_end, stream);
     int launches = 1;
     if (e == cudaSuccess && splits > 1) {

@@ -24,8 +24,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const AttnParams p) {
     const long long row = (long long)blockIdx.x * 8 + warp;
     if (row >= rows) return;
     const int S = p.num_splits;
-    float mx = -CUDART_INF_F;
-    for (int s = lane; s < S; s += 32) mx = fmaxf(mx, p.ws_lse[(size_t)s * rows + row]);
+    // Lane l holds the log2-sum-exp of splits l, l+32, ... (all loads in flight at once).
+    float lse_l[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int s = lane + 32 * k;
+        lse_l[k] = s < S ? p.ws_lse[(size_t)s * rows + row] : -CUDART_INF_F;
+    }
+    float mx = fmaxf(fmaxf(lse_l[0], lse_l[1]), fmaxf(lse_l[2], lse_l[3]));
+    for (int s = lane + 128; s < S; s += 32) mx = fmaxf(mx, p.ws_lse[(size_t)s * rows + row]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     float acc[V];
@@ -33,22 +40,40 @@ __global__ void __launch_bounds__(256) combine_kernel(const AttnParams p) {
     for (int i = 0; i < V; ++i) acc[i] = 0.f;
     if (mx != -CUDART_INF_F) {
         float L = 0.f;
-        for (int s = 0; s < S; ++s) {
-            const float lse = p.ws_lse[(size_t)s * rows + row];
-            if (lse == -CUDART_INF_F) continue;
-            const float w = ex2(lse - mx);
-            L += w;
-            const float* src = p.ws_o + ((size_t)s * rows + row) * D + lane * V;
-            if constexpr (V == 4) {
-                const float4 v = *reinterpret_cast<const float4*>(src);
-                acc[0] = fmaf(w, v.x, acc[0]);
-                acc[1] = fmaf(w, v.y, acc[1]);
-                acc[2] = fmaf(w, v.z, acc[2]);
-                acc[3] = fmaf(w, v.w, acc[3]);
-            } else {
-                const float2 v = *reinterpret_cast<const float2*>(src);
-                acc[0] = fmaf(w, v.x, acc[0]);
-                acc[1] = fmaf(w, v.y, acc[1]);
+        const float* base = p.ws_o + (size_t)row * D + lane * V;
+        const size_t split_stride = (size_t)rows * D;
+        for (int s0 = 0; s0 < S; s0 += 32) {
+            // weights of splits s0..s0+31, one per lane
+            const int k = s0 >> 5;
+            float lse;
+            if (k == 0)
+                lse = lse_l[0];
+            else if (k == 1)
+                lse = lse_l[1];
+            else if (k == 2)
+                lse = lse_l[2];
+            else if (k == 3)
+                lse = lse_l[3];
+            else
+                lse = s0 + lane < S ? p.ws_lse[(size_t)(s0 + lane) * rows + row] : -CUDART_INF_F;
+            const float w_l = lse == -CUDART_INF_F ? 0.f : ex2(lse - mx);
+            const int n = min(32, S - s0);
+#pragma unroll 8
+            for (int j = 0; j < n; ++j) {
+                const float w = __shfl_sync(0xffffffffu, w_l, j);
+                L += w;
+                const float* src = base + (size_t)(s0 + j) * split_stride;
+                if constexpr (V == 4) {
+                    const float4 v = *reinterpret_cast<const float4*>(src);
+                    acc[0] = fmaf(w, v.x, acc[0]);
+                    acc[1] = fmaf(w, v.y, acc[1]);
+                    acc[2] = fmaf(w, v.z, acc[2]);
+                    acc[3] = fmaf(w, v.w, acc[3]);
+                } else {
+                    const float2 v = *reinterpret_cast<const float2*>(src);
+                    acc[0] = fmaf(w, v.x, acc[0]);
+                    acc[1] = fmaf(w, v.y, acc[1]);
+                }
             }
         }
         const float inv = 1.f / L;

@@ -2,16 +2,21 @@
 // 64 GQA-packed query rows (query token i, head g*G + r packed as row i*G + r),
 // so every K/V byte of a kv head is read from HBM once per split.
 //
-// Pipeline: one producer warp issues TMA tile loads of 16-key page slices
-// (box 64 dims x 1 head x 16 slots x 1 block, 128-byte swizzle) into an
-// nstage-deep ring of K/V stages; consumer warps wait on the stage's full
-// mbarrier, run QK^T and PV on bf16 mma.sync (fp32 accumulate), apply the
-// scale, the sheared relative bias and the mask per element, keep an fp32
-// online softmax, and release the stage.  Warps split the stage's keys
-// (KSL slices of 16) and the rows (MT tiles of 16); their partial (m, l, O)
-// merge through shared memory at the end.  With one split the result is
-// written as bf16; otherwise the fp32 O/l and log2-sum-exp go to the
-// workspace for the combine kernel.
+// The CTA's key range (this split's share of the request's visible keys) is
+// cut into stages of 16*KSL keys.  Producer warps gather each stage from
+// the paged cache with 16-byte cp.async (one block-table lookup per 16-key
+// page slice, keys past the visible range zero-filled) into a ring of NSTAGE
+// slots whose rows are padded by 16 bytes, so the ldmatrix reads are
+// conflict-free; completion is signalled on the slot's mbarrier by
+// cp.async.mbarrier.arrive.  KSL x MT consumer warps each take one 16-key
+// slice of a stage and one 16-row tile: QK^T and PV on bf16 mma.sync with
+// fp32 accumulation, the scale, the sheared relative bias and the mask per
+// element (skipped for slices wholly visible and outside the bias band), and
+// an fp32 online softmax in base 2; then they release the slot.  The
+// consumers' (m, l, O) merge through shared memory at the end.  With one
+// split the result is written directly (bf16 or fp32); otherwise the
+// normalised fp32 partial and its log2-sum-exp go to the workspace for the
+// combine kernel.  Every mbarrier wait is bounded.
 //
 // Semantics: vLLM API docs, inkling_fa4_rel_attention (paged varlen forward);
 // bias rule: prhub report on vLLM PR #48858, score_mod_rel_bias.
@@ -29,33 +34,30 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D, int MT, int KSL>
 struct DecodeCfg {
-    static constexpr int kWarps = MT * KSL;              // consumer warps
-    static constexpr int kThreads = (kWarps + 1) * 32;   // + one producer warp
+    static constexpr int kConsumers = MT * KSL;
+    static constexpr int kMaxProducers = 4;
+    static constexpr int kMaxThreads = (kConsumers + kMaxProducers) * 32;
     static constexpr int kStageKeys = 16 * KSL;
-    static constexpr int kHalves = D / 64;               // 64-dim swizzled column blocks
-    static constexpr int kHalfBytes = kStageKeys * 128;  // one column block of one operand
-    static constexpr int kStageBytes = 2 * kHalves * kHalfBytes;
-    static constexpr int kRedStride = D + 4;             // floats per row in the merge area
+    // A stage holds kStageKeys K rows then as many V rows; each row is padded
+    // by 16 bytes so the 8 rows an ldmatrix reads fall in distinct banks.
+    static constexpr int kRowBytes = D * 2 + 16;
+    static constexpr int kOperandBytes = kStageKeys * kRowBytes;
+    static constexpr int kStageBytes = 2 * kOperandBytes;
+    static constexpr int kChunks = D / 8;            // 16-byte chunks per key row
+    static constexpr int kRowsPerCopy = 32 / kChunks;  // rows one warp-wide copy covers
+    static constexpr int kRedStride = D + 4;         // floats per row in the merge area
     static constexpr int kRedBytes = KSL * MT * 16 * (kRedStride + 2) * 4;
-    static constexpr int kMaxStages = 16;
-};
-
-struct RowInfo {
-    int valid;
-    int pos;                   // key position of the query row
-    const uint16_t* rel;       // rel_logits row (t, h, :)
+    static constexpr int kMaxStages = 12;
 };
 
 template <int D, int MT, int KSL>
-__global__ void __launch_bounds__(DecodeCfg<D, MT, KSL>::kThreads)
-decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-              const AttnParams p) {
+__global__ void __launch_bounds__(DecodeCfg<D, MT, KSL>::kMaxThreads) decode_kernel(const AttnParams p) {
     using C = DecodeCfg<D, MT, KSL>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int nstage = p.nstage;
-    const size_t body = (size_t)nstage * C::kStageBytes > (size_t)C::kRedBytes ? (size_t)nstage * C::kStageBytes
-                                                                                : (size_t)C::kRedBytes;
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    const int NST = p.nstage;
+    const size_t body = (size_t)NST * C::kStageBytes > (size_t)C::kRedBytes ? (size_t)NST * C::kStageBytes
+                                                                             : (size_t)C::kRedBytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + body);
     uint64_t* empty = full + C::kMaxStages;
     int* abort_flag = reinterpret_cast<int*>(empty + C::kMaxStages);
@@ -71,7 +73,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     if (n_rows <= 0) return;
     const int off = sk - sq;
 
-    // Keys any row of this request may see, cut into stage tiles and split.
+    // Keys any row of this request may see, cut into stages and split.
     int khi = sk;
     if (p.causal) khi = min(khi, sq + off);
     if (p.wr >= 0) khi = min(khi, sq + off + p.wr);
@@ -89,116 +91,117 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     const int n_it = t_end - t_begin;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < nstage; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], C::kWarps);
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(&full[i], 32 * p.nprod);     // one arrival per producer lane
+            mbar_init(&empty[i], C::kConsumers);  // one arrival per consumer warp
         }
         *abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
 
-    auto k_half = [&](int slot, int hh) { return smem + (size_t)slot * C::kStageBytes + hh * C::kHalfBytes; };
-    auto v_half = [&](int slot, int hh) {
-        return smem + (size_t)slot * C::kStageBytes + (C::kHalves + hh) * C::kHalfBytes;
-    };
-
-    if (warp == C::kWarps) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
-        }
-        const uint64_t policy = l2_policy_evict_first();
-        const int nblk_needed = min((khi + p.BS - 1) / p.BS, p.max_blocks);
+    if (warp >= C::kConsumers) {
+        // ----------------------------------------------------------- producers
+        // Producer warp pw gathers pages pw, pw + nprod, ... of every stage.
+        const int pw = warp - C::kConsumers, nprod = p.nprod;
+        const uint16_t* kc = reinterpret_cast<const uint16_t*>(p.k_cache);
+        const uint16_t* vc = reinterpret_cast<const uint16_t*>(p.v_cache);
         const int32_t* bt = p.block_table + (size_t)b * p.bt_stride;
+        const int nblk = min((khi + p.BS - 1) / p.BS, p.max_blocks);
+        const uint64_t policy = l2_policy_evict_first();
+        // This lane copies 16-byte chunk `cchunk` of rows crow, crow + kRowsPerCopy, ...
+        const int crow = lane / C::kChunks, cchunk = lane % C::kChunks;
+        const size_t lane_off = (size_t)crow * p.c_s1 + cchunk * 8 + (size_t)g * p.c_s2;
+        const uint32_t lane_dst = crow * C::kRowBytes + cchunk * 16;
         int cached_base = -(1 << 30);
-        int my_blk = -1;
+        int my_blk = 0;
         for (int it = 0; it < n_it; ++it) {
-            const int slot = it % nstage;
-            const int round = it / nstage;
-            const int k0 = kstart + (t_begin + it) * BN;
+            const int slot = it % NST;
+            const int round = it / NST;
             bool ok = true;
             if (lane == 0) ok = mbar_wait(&empty[slot], (round & 1) ^ 1, p.timeout_ns, kSiteDecodeEmpty, p.err);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
-            int nvalid = 0;
-#pragma unroll
-            for (int u = 0; u < KSL; ++u) nvalid += (k0 + 16 * u < khi) ? 1 : 0;
-            if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)(nvalid * 2 * C::kHalves * 2048));
-#pragma unroll
-            for (int u = 0; u < KSL; ++u) {
-                const int j = k0 + 16 * u;
-                if (j >= khi) break;  // warp-uniform
-                const int n = j / p.BS;
-                if (n - cached_base >= 32 || n < cached_base) {
+            const int k0 = kstart + (t_begin + it) * BN;
+            const uint32_t dst_stage = smem_u32(smem + (size_t)slot * C::kStageBytes) + lane_dst;
+            for (int pg = pw; pg < KSL; pg += nprod) {
+                const int j0 = k0 + 16 * pg;
+                const int n = j0 / p.BS;
+                if (n - cached_base >= 32 || n < cached_base) {  // warp-uniform
                     cached_base = n;
-                    my_blk = (n + lane < nblk_needed) ? bt[n + lane] : -1;
+                    my_blk = (n + lane < nblk) ? __ldg(bt + n + lane) : 0;
                 }
-                const int blk = __shfl_sync(0xffffffffu, my_blk, n - cached_base);
-                if (lane == 0) {
-                    const int slot_in_blk = j - n * p.BS;
+                // A block id outside [0, NB) breaks the caller's contract; clamp
+                // it so the gather stays inside the cache instead of faulting.
+                const int blk = min(max(__shfl_sync(0xffffffffu, my_blk, n - cached_base), 0), p.NB - 1);
+                const size_t page = (size_t)blk * p.c_s0 + (size_t)(j0 - n * p.BS) * p.c_s1 + lane_off;
+                const bool full_pg = j0 + 16 <= khi;
 #pragma unroll
-                    for (int hh = 0; hh < C::kHalves; ++hh) {
-                        tma_load_4d_hint(k_half(slot, hh) + u * 2048, &tmK, &full[slot], hh * 64, g, slot_in_blk,
-                                         blk, policy);
-                        tma_load_4d_hint(v_half(slot, hh) + u * 2048, &tmV, &full[slot], hh * 64, g, slot_in_blk,
-                                         blk, policy);
-                    }
+                for (int r = 0; r < 16 / C::kRowsPerCopy; ++r) {
+                    const int row = r * C::kRowsPerCopy;  // + crow
+                    const bool okr = full_pg || j0 + row + crow < khi;
+                    const size_t src = page + (size_t)row * p.c_s1;
+                    const uint32_t dst = dst_stage + (16 * pg + row) * C::kRowBytes;
+                    cp_async_16(dst, okr ? kc + src : kc, okr ? 16u : 0u, policy);
+                    cp_async_16(dst + C::kOperandBytes, okr ? vc + src : vc, okr ? 16u : 0u, policy);
                 }
             }
+            cp_async_arrive_noinc(&full[slot]);
         }
+        cp_async_wait(0);
         return;
     }
 
     // ---------------------------------------------------------------- consumers
-    const int mt = warp % MT, ks = warp / MT;
+    const int mt = warp % MT, ks = warp / MT;  // row tile, 16-key slice of each stage
+
+    // ------------------------------------------------------------- rows
     const int gq = lane >> 2, tig = lane & 3;
-    const int rloc[2] = {mt * 16 + gq, mt * 16 + gq + 8};
-    RowInfo ri[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        const int r = rloc[e];
-        ri[e].valid = r < n_rows;
-        const int qi = ri[e].valid ? r / G : 0;
-        const int hh = ri[e].valid ? r % G : 0;
-        ri[e].pos = qi + off;
-        const int t = q0 + qi, h = g * G + hh;
-        ri[e].rel = p.R > 0 ? reinterpret_cast<const uint16_t*>(p.rel) + ((size_t)t * p.H + h) * p.R : nullptr;
+    const int r0 = mt * 16 + gq, r1 = r0 + 8;
+    const bool valid0 = r0 < n_rows, valid1 = r1 < n_rows;
+    const int qi0 = valid0 ? r0 / G : 0, qi1 = valid1 ? r1 / G : 0;
+    const int pos0 = qi0 + off, pos1 = qi1 + off;  // key positions of the two rows
+    const int h0 = g * G + (valid0 ? r0 % G : 0), h1 = g * G + (valid1 ? r1 % G : 0);
+    const uint16_t* rel0 = nullptr;
+    const uint16_t* rel1 = nullptr;
+    if (p.R > 0) {
+        rel0 = reinterpret_cast<const uint16_t*>(p.rel) + ((size_t)(q0 + qi0) * p.H + h0) * p.R;
+        rel1 = reinterpret_cast<const uint16_t*>(p.rel) + ((size_t)(q0 + qi1) * p.H + h1) * p.R;
     }
+    // Extreme key positions over the CTA's valid rows (rows are token-major).
+    const int pos_lo = off, pos_hi = (n_rows - 1) / G + off;
 
     // Q fragments (A operand, rows x dims), loaded once.
     uint32_t qf[D / 16][4];
     {
         const uint16_t* qb = reinterpret_cast<const uint16_t*>(p.q);
-        const uint32_t* rowp[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int r = ri[e].valid ? rloc[e] : 0;
-            const int t = q0 + r / G, h = g * G + r % G;
-            rowp[e] = reinterpret_cast<const uint32_t*>(qb + (size_t)t * p.q_st + (size_t)h * p.q_sh);
-        }
+        const uint32_t* rowp0 =
+            reinterpret_cast<const uint32_t*>(qb + (size_t)(q0 + qi0) * p.q_st + (size_t)h0 * p.q_sh);
+        const uint32_t* rowp1 =
+            reinterpret_cast<const uint32_t*>(qb + (size_t)(q0 + qi1) * p.q_st + (size_t)h1 * p.q_sh);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-            qf[kk][0] = ri[0].valid ? __ldg(rowp[0] + kk * 8 + tig) : 0u;
-            qf[kk][1] = ri[1].valid ? __ldg(rowp[1] + kk * 8 + tig) : 0u;
-            qf[kk][2] = ri[0].valid ? __ldg(rowp[0] + kk * 8 + 4 + tig) : 0u;
-            qf[kk][3] = ri[1].valid ? __ldg(rowp[1] + kk * 8 + 4 + tig) : 0u;
+            qf[kk][0] = valid0 ? __ldg(rowp0 + kk * 8 + tig) : 0u;
+            qf[kk][1] = valid1 ? __ldg(rowp1 + kk * 8 + tig) : 0u;
+            qf[kk][2] = valid0 ? __ldg(rowp0 + kk * 8 + 4 + tig) : 0u;
+            qf[kk][3] = valid1 ? __ldg(rowp1 + kk * 8 + 4 + tig) : 0u;
         }
     }
 
     float o[D / 8][4];
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    for (int a = 0; a < D / 8; ++a) o[a][0] = o[a][1] = o[a][2] = o[a][3] = 0.f;
+    // m_run: running maximum of each row (log2 domain).  O and l are rescaled
+    // only in slices where some row of the warp raised its maximum; the row's
+    // largest p is then exactly 1, so its bf16 rounding is exact.
     float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};
     float l_run[2] = {0.f, 0.f};
     const float sl2 = p.scale_log2;
     const int R = p.R, wl = p.wl, wr = p.wr, causal = p.causal;
 
     for (int it = 0; it < n_it; ++it) {
-        const int slot = it % nstage;
-        const int round = it / nstage;
-        const int jb = kstart + (t_begin + it) * BN + ks * 16;  // this warp's first key
+        const int slot = it % NST;
+        const int round = it / NST;
         bool ok = true;
         if (lane == 0) ok = mbar_wait(&full[slot], round & 1, p.timeout_ns, kSiteDecodeFull, p.err);
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -206,66 +209,97 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             if (lane == 0) *abort_flag = 1;
             break;
         }
-        // Keys at or past khi hold stale or unloaded data: zero their V rows so
-        // that p = 0 times them stays 0.
-        if (jb + 16 > khi) {
-            const int first = max(0, khi - jb);
-            for (int idx = lane; idx < (16 - first) * 8 * C::kHalves; idx += 32) {
-                const int row = first + idx / (8 * C::kHalves);
-                const int rem = idx % (8 * C::kHalves);
-                uint8_t* base = v_half(slot, rem / 8) + (ks * 16 + row) * 128 + (rem % 8) * 16;
-                *reinterpret_cast<uint4*>(base) = make_uint4(0, 0, 0, 0);
-            }
-            __syncwarp();
-        }
+        const uint8_t* kbuf = smem + (size_t)slot * C::kStageBytes + ks * 16 * C::kRowBytes;
+        const uint8_t* vbuf = kbuf + C::kOperandBytes;
+        const int jb = kstart + (t_begin + it) * BN + ks * 16;  // this warp's first key
 
-        // S = Q K^T over this warp's 16 keys: two n-tiles of 8 keys.
-        float sacc[2][4];
+        // S = Q K^T over the slice: two n-tiles of 8 keys, each accumulated in
+        // two halves of the head dim to shorten the MMA chains.
+        float sacc[2][4], sacc2[2][4];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[a][e] = sacc2[a][e] = 0.f;
         {
-            const int krow = ks * 16 + (lane >> 4) * 8 + (lane & 7);
+            const int krow = (lane >> 4) * 8 + (lane & 7);
             const int csel = (lane >> 3) & 1;
+            const uint32_t kb = smem_u32(kbuf) + krow * C::kRowBytes + csel * 16;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t addr =
-                    smem_u32(k_half(slot, kk >> 2)) + sw128_offset(krow, (kk & 3) * 2 + csel);
+                const uint32_t addr = kb + kk * 32;
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4(addr, b0, b1, b2, b3);
-                mma_bf16_16816(sacc[0], qf[kk], b0, b1);
-                mma_bf16_16816(sacc[1], qf[kk], b2, b3);
+                if (kk & 1) {
+                    mma_bf16_16816(sacc2[0], qf[kk], b0, b1);
+                    mma_bf16_16816(sacc2[1], qf[kk], b2, b3);
+                } else {
+                    mma_bf16_16816(sacc[0], qf[kk], b0, b1);
+                    mma_bf16_16816(sacc[1], qf[kk], b2, b3);
+                }
             }
         }
 
-        // Scale, sheared bias, mask.
+        // Scale, sheared bias, mask.  Warp-uniform fast path: every key of the
+        // slice is visible to every row and no row's distance reaches the band.
+        const bool all_visible = jb + 16 <= khi && (!causal || jb + 15 <= pos_lo) &&
+                                 (wl < 0 || jb >= pos_hi - wl) && (wr < 0 || jb + 15 <= pos_lo + wr);
+        const bool no_bias = R == 0 || pos_lo - (jb + 15) >= R || pos_hi - jb < 0;
         float s[2][4];
+        if (all_visible && no_bias) {
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+            for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const RowInfo& rr = ri[e >> 1];
-                const int j = jb + nt * 8 + 2 * tig + (e & 1);
-                const int d = rr.pos - j;
-                bool allowed = rr.valid && j < khi;
-                if (causal) allowed = allowed && d >= 0;
-                if (wl >= 0) allowed = allowed && d <= wl;
-                if (wr >= 0) allowed = allowed && d >= -wr;
-                float bias = 0.f;
-                if (allowed && d >= 0 && d < R) bias = bf16_bits_to_f32(__ldg(rr.rel + d));
-                s[nt][e] = allowed ? fmaf(sacc[nt][e], sl2, bias * kLog2e) : -CUDART_INF_F;
+                for (int e = 0; e < 4; ++e) s[nt][e] = (sacc[nt][e] + sacc2[nt][e]) * sl2;
+        } else {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const bool second = e >> 1;
+                    const int pos = second ? pos1 : pos0;
+                    const uint16_t* relr = second ? rel1 : rel0;
+                    const int j = jb + nt * 8 + 2 * tig + (e & 1);
+                    const int d = pos - j;
+                    bool allowed = (second ? valid1 : valid0) && j < khi;
+                    if (causal) allowed = allowed && d >= 0;
+                    if (wl >= 0) allowed = allowed && d <= wl;
+                    if (wr >= 0) allowed = allowed && d >= -wr;
+                    float bias = 0.f;
+                    if (allowed && d >= 0 && d < R) bias = bf16_bits_to_f32(__ldg(relr + d));
+                    s[nt][e] = allowed ? fmaf(sacc[nt][e] + sacc2[nt][e], sl2, bias * kLog2e) : -CUDART_INF_F;
+                }
             }
         }
 
         // Online softmax (base 2).  Rows gq (e = 0,1) and gq + 8 (e = 2,3).
-        float alpha[2];
+        float mx[2];
 #pragma unroll
         for (int rsel = 0; rsel < 2; ++rsel) {
-            float mx = fmaxf(fmaxf(s[0][2 * rsel], s[0][2 * rsel + 1]), fmaxf(s[1][2 * rsel], s[1][2 * rsel + 1]));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const float m_new = fmaxf(m_run[rsel], mx);
-            const float mu = m_new == -CUDART_INF_F ? 0.f : m_new;
-            alpha[rsel] = ex2(m_run[rsel] - mu);
+            float v = fmaxf(fmaxf(s[0][2 * rsel], s[0][2 * rsel + 1]), fmaxf(s[1][2 * rsel], s[1][2 * rsel + 1]));
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+            mx[rsel] = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+        }
+        const bool grow = mx[0] > m_run[0] || mx[1] > m_run[1];
+        if (__any_sync(0xffffffffu, grow)) {
+            float alpha[2];
+#pragma unroll
+            for (int rsel = 0; rsel < 2; ++rsel) {
+                const float m_new = fmaxf(m_run[rsel], mx[rsel]);
+                alpha[rsel] = m_new == -CUDART_INF_F ? 1.f : ex2(m_run[rsel] - m_new);
+                l_run[rsel] *= alpha[rsel];
+                m_run[rsel] = m_new;
+            }
+#pragma unroll
+            for (int a = 0; a < D / 8; ++a) {
+                o[a][0] *= alpha[0];
+                o[a][1] *= alpha[0];
+                o[a][2] *= alpha[1];
+                o[a][3] *= alpha[1];
+            }
+        }
+#pragma unroll
+        for (int rsel = 0; rsel < 2; ++rsel) {
+            const float mu = m_run[rsel] == -CUDART_INF_F ? 0.f : m_run[rsel];
             float rs = 0.f;
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
@@ -273,37 +307,29 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
                 s[nt][2 * rsel + 1] = ex2(s[nt][2 * rsel + 1] - mu);
                 rs += s[nt][2 * rsel] + s[nt][2 * rsel + 1];
             }
-            l_run[rsel] = l_run[rsel] * alpha[rsel] + rs;
-            m_run[rsel] = m_new;
-        }
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i) {
-            o[i][0] *= alpha[0];
-            o[i][1] *= alpha[0];
-            o[i][2] *= alpha[1];
-            o[i][3] *= alpha[1];
+            l_run[rsel] += rs;
         }
 
-        // O += P V.
+        // O += P V.  Keys past the visible range were zero-filled, so their
+        // V rows contribute 0 * 0.
         uint32_t pa[4];
         pa[0] = pack_bf16(s[0][0], s[0][1]);
         pa[1] = pack_bf16(s[0][2], s[0][3]);
         pa[2] = pack_bf16(s[1][0], s[1][1]);
         pa[3] = pack_bf16(s[1][2], s[1][3]);
         {
-            const int vrow = ks * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+            const int vrow = ((lane >> 3) & 1) * 8 + (lane & 7);
             const int csel = lane >> 4;
+            const uint32_t vb = smem_u32(vbuf) + vrow * C::kRowBytes + csel * 16;
 #pragma unroll
             for (int n2 = 0; n2 < D / 16; ++n2) {
-                const uint32_t addr =
-                    smem_u32(v_half(slot, n2 >> 2)) + sw128_offset(vrow, (n2 & 3) * 2 + csel);
+                const uint32_t addr = vb + n2 * 32;
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4_t(addr, b0, b1, b2, b3);
                 mma_bf16_16816(o[2 * n2], pa, b0, b1);
                 mma_bf16_16816(o[2 * n2 + 1], pa, b2, b3);
             }
         }
-        if (jb + 16 > khi) fence_proxy_async_smem();  // generic zeroing before the next TMA write
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
     }
@@ -315,30 +341,30 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         l_run[rsel] += __shfl_xor_sync(0xffffffffu, l_run[rsel], 2);
     }
 
-    // Merge the KSL key slices through shared memory (stage buffers are free:
-    // every issued stage was waited on by every consumer warp).
-    asm volatile("bar.sync 1, %0;" ::"r"(C::kWarps * 32) : "memory");
-    if (*(volatile int*)abort_flag) return;  // CTA-uniform: every consumer warp sees it
+    // Merge the key slices through shared memory (every stage was waited on by
+    // every consumer warp, so all copies into the ring have landed).
+    asm volatile("bar.sync 1, %0;" ::"r"(C::kConsumers * 32) : "memory");
+    if (*(volatile int*)abort_flag) return;  // CTA-uniform after the barrier
     float* red_o = reinterpret_cast<float*>(smem);
     float* red_m = red_o + KSL * MT * 16 * C::kRedStride;
     float* red_l = red_m + KSL * MT * 16;
     const int rows_cta = MT * 16;
 #pragma unroll
     for (int rsel = 0; rsel < 2; ++rsel) {
-        const int r = rloc[rsel];
+        const int r = rsel ? r1 : r0;
         float* dst = red_o + ((size_t)ks * rows_cta + r) * C::kRedStride;
 #pragma unroll
-        for (int i = 0; i < D / 8; ++i)
-            *reinterpret_cast<float2*>(dst + i * 8 + 2 * tig) = make_float2(o[i][2 * rsel], o[i][2 * rsel + 1]);
+        for (int a = 0; a < D / 8; ++a)
+            *reinterpret_cast<float2*>(dst + a * 8 + 2 * tig) = make_float2(o[a][2 * rsel], o[a][2 * rsel + 1]);
         if (tig == 0) {
             red_m[ks * rows_cta + r] = m_run[rsel];
             red_l[ks * rows_cta + r] = l_run[rsel];
         }
     }
-    asm volatile("bar.sync 1, %0;" ::"r"(C::kWarps * 32) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"r"(C::kConsumers * 32) : "memory");
 
     const bool partial = p.num_splits > 1;
-    for (int idx = threadIdx.x; idx < rows_cta * (D / 4); idx += C::kWarps * 32) {
+    for (int idx = threadIdx.x; idx < rows_cta * (D / 4); idx += C::kConsumers * 32) {
         const int r = idx / (D / 4), c4 = idx % (D / 4);
         if (r >= n_rows) continue;
         float M = -CUDART_INF_F;
@@ -351,7 +377,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
             for (int k = 0; k < KSL; ++k) {
                 const float w = ex2(red_m[k * rows_cta + r] - M);
                 L += w * red_l[k * rows_cta + r];
-                const float4 v = *reinterpret_cast<const float4*>(red_o + ((size_t)k * rows_cta + r) * C::kRedStride + c4 * 4);
+                const float4 v =
+                    *reinterpret_cast<const float4*>(red_o + ((size_t)k * rows_cta + r) * C::kRedStride + c4 * 4);
                 acc.x += w * v.x;
                 acc.y += w * v.y;
                 acc.z += w * v.z;
@@ -384,83 +411,83 @@ decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
 }
 
 template <int D, int MT, int KSL>
-int decode_smem_bytes(int nstage) {
+int decode_smem_bytes(int nst) {
     using C = DecodeCfg<D, MT, KSL>;
-    int body = nstage * C::kStageBytes;
+    int body = nst * C::kStageBytes;
     if (body < C::kRedBytes) body = C::kRedBytes;
-    return 1024 + body + 2 * C::kMaxStages * 8 + 16;
+    return 128 + body + 2 * C::kMaxStages * 8 + 16;
 }
 
 template <int D, int MT, int KSL>
-int pick_nstage(int ctas, int num_sms) {
+int pick_stages(int ctas, int num_sms) {
     using C = DecodeCfg<D, MT, KSL>;
-    // One CTA per SM when the grid fits in one wave, else two per SM.
-    const int budget = (ctas <= num_sms) ? 200 * 1024 : 100 * 1024;
-    int n = budget / C::kStageBytes;
+    // One CTA per SM when the grid fits in one wave, else two per SM; the
+    // ring takes what shared memory allows so the producer runs far ahead.
+    const int budget = (ctas <= num_sms) ? 224 * 1024 : 111 * 1024;
+    int n = (budget - 512) / C::kStageBytes;
     if (n > C::kMaxStages) n = C::kMaxStages;
     if (n < 2) n = 2;
     return n;
 }
 
 template <int D, int MT, int KSL>
-cudaError_t launch_t(const AttnParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, const LaunchShape& s,
-                     cudaStream_t stream) {
+cudaError_t launch_t(const AttnParams& p, const LaunchShape& s, cudaStream_t stream) {
     auto kern = decode_kernel<D, MT, KSL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, s.smem);
     if (e != cudaSuccess) return e;
-    kern<<<s.grid, s.block, s.smem, stream>>>(tmK, tmV, p);
+    kern<<<s.grid, s.block, s.smem, stream>>>(p);
     return cudaGetLastError();
-}
-
-void tile_choice(int rows, int& mt, int& ksl) {
-    if (rows <= 16) {
-        mt = 1;
-        ksl = 4;
-    } else if (rows <= 32) {
-        mt = 2;
-        ksl = 4;
-    } else {
-        mt = 4;
-        ksl = 2;
-    }
 }
 
 }  // namespace
 
+// Tile shape: up to 16 packed rows use one 16-row MMA tile and 8 key groups
+// (8 warps) when the grid fits in one wave, else 4 groups so that two CTAs
+// share an SM; 17-32 rows use 2 row tiles x 4 groups, 33-64 rows 4 x 2.
 LaunchShape decode_shape(const AttnParams& p, int num_sms) {
     LaunchShape s;
-    int mt, ksl;
-    tile_choice(p.max_rows, mt, ksl);
-    s.grid = dim3(p.num_splits, p.Hk, p.B);
-    s.block = (mt * ksl + 1) * 32;
     const int ctas = p.num_splits * p.Hk * p.B;
-    int nst = 2;
+    if (p.max_rows <= 16) {
+        s.mt = 1;
+        s.ksl = ctas <= num_sms ? 8 : 4;
+    } else if (p.max_rows <= 32) {
+        s.mt = 2;
+        s.ksl = 4;
+    } else {
+        s.mt = 4;
+        s.ksl = 2;
+    }
+    s.grid = dim3(p.num_splits, p.Hk, p.B);
+    // Two producer warps per CTA, four when one CTA owns the SM: a single
+    // issuing warp cannot keep enough 16-byte gathers in flight.
+    s.nprod = s.mt * s.ksl >= 8 ? 4 : 2;
+    s.block = (s.mt * s.ksl + s.nprod) * 32;
 #define REL_ATTN_SHAPE(DD, M, K)                         \
-    if (p.D == DD && mt == M && ksl == K) {             \
-        nst = pick_nstage<DD, M, K>(ctas, num_sms);     \
-        s.smem = decode_smem_bytes<DD, M, K>(nst);      \
+    if (p.D == DD && s.mt == M && s.ksl == K) {         \
+        s.nstage = pick_stages<DD, M, K>(ctas, num_sms); \
+        s.smem = decode_smem_bytes<DD, M, K>(s.nstage); \
     }
     REL_ATTN_SHAPE(64, 1, 4)
+    REL_ATTN_SHAPE(64, 1, 8)
     REL_ATTN_SHAPE(64, 2, 4)
     REL_ATTN_SHAPE(64, 4, 2)
     REL_ATTN_SHAPE(128, 1, 4)
+    REL_ATTN_SHAPE(128, 1, 8)
     REL_ATTN_SHAPE(128, 2, 4)
     REL_ATTN_SHAPE(128, 4, 2)
 #undef REL_ATTN_SHAPE
-    s.nstage = nst;
     return s;
 }
 
-cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                          const LaunchShape& s, cudaStream_t stream) {
-    int mt, ksl;
-    tile_choice(p.max_rows, mt, ksl);
+cudaError_t launch_decode(const AttnParams& p, const LaunchShape& s, cudaStream_t stream) {
 #define REL_ATTN_LAUNCH(DD, M, K) \
-    if (p.D == DD && mt == M && ksl == K) return launch_t<DD, M, K>(p, tmK, tmV, s, stream);
+    if (p.D == DD && s.mt == M && s.ksl == K) return launch_t<DD, M, K>(p, s, stream);
     REL_ATTN_LAUNCH(64, 1, 4)
+    REL_ATTN_LAUNCH(64, 1, 8)
     REL_ATTN_LAUNCH(64, 2, 4)
     REL_ATTN_LAUNCH(64, 4, 2)
     REL_ATTN_LAUNCH(128, 1, 4)
+    REL_ATTN_LAUNCH(128, 1, 8)
     REL_ATTN_LAUNCH(128, 2, 4)
     REL_ATTN_LAUNCH(128, 4, 2)
 #undef REL_ATTN_LAUNCH

@@ -11,6 +11,10 @@ namespace relattn {
 struct AttnParams {
     const void* q;             // (T, H, D) bf16
     int64_t q_st, q_sh;        // token / head strides
+    const void* k_cache;       // (NB, BS, Hk, D) bf16
+    const void* v_cache;
+    int64_t c_s0, c_s1, c_s2;  // cache block / slot / head strides (shared by K and V)
+    int32_t NB;
     const int32_t* block_table;
     int64_t bt_stride;         // MB
     int32_t max_blocks;        // MB
@@ -30,6 +34,7 @@ struct AttnParams {
     float scale_log2;          // softmax_scale * log2(e)
     int32_t causal, wl, wr;
     int32_t nstage;
+    int32_t nprod;             // decode: producer warps
     uint64_t timeout_ns;
     int* err;                  // device error word (bounded-wait timeouts)
 };
@@ -39,12 +44,13 @@ struct LaunchShape {
     int block = 0;
     int smem = 0;
     int nstage = 0;
+    int mt = 0, ksl = 0;  // decode: 16-row tiles and 16-key slices per CTA
+    int nprod = 1;        // decode: producer warps
 };
 
 // Split-KV decode kernel for <= 64 GQA-packed rows per (request, kv head).
 LaunchShape decode_shape(const AttnParams& p, int num_sms);
-cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                          const LaunchShape& shape, cudaStream_t stream);
+cudaError_t launch_decode(const AttnParams& p, const LaunchShape& shape, cudaStream_t stream);
 
 // LSE-weighted merge of split partials into bf16 out.
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t stream);
