@@ -134,6 +134,55 @@ rel_attn_status rel_attn_paged_varlen(
     rel_attn_stream stream);
 
 /*
+ * rel_attn_paged_varlen_noalloc - the same forward for the decode path
+ * (max_seqlen_q * num_heads / num_kv_heads <= 64) that allocates no device
+ * memory.  It has no counterpart on the pages that define the attention; it
+ * exists for callers that cannot allocate: a framework that owns the device
+ * through its own memory pool (a second allocator working behind its back can
+ * run out of memory while the pool holds nearly all of the device, or
+ * fragment it), or a program that allocates everything at start-up and
+ * forbids allocation afterwards.
+ *
+ * Arguments, results and errors are those of rel_attn_paged_varlen.  The
+ * caller still provides every input and the output.  The split-KV workspace
+ * (num_splits * T * H * (D + 1) * 4 bytes, after num_splits is clamped) comes
+ * from a fixed array of REL_ATTN_NOALLOC_SCRATCH_BYTES bytes inside the
+ * library; every GPU that loads the library holds one such array until the
+ * process exits.  A call whose workspace would not fit returns
+ * REL_ATTN_ERR_INVALID_ARGUMENT with a message naming both sizes, before any
+ * device work; so does a call on the prefill path
+ * (REL_ATTN_ERR_UNSUPPORTED).  It calls no cudaMalloc, cudaMallocAsync,
+ * cudaFree or other allocating routine.
+ *
+ * The first call on each device looks up the device address of the array
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls share the one array and it keeps the
+ * last call's contents; nothing in it needs to start at zero, since every
+ * value the combine step reads is written earlier in the same call.  Calls
+ * that use more than one split and overlap on the GPU (other streams, other
+ * host threads) race on the array: order them on one stream.
+ */
+#define REL_ATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+rel_attn_status rel_attn_paged_varlen_noalloc(
+    const rel_attn_tensor* q,
+    const rel_attn_tensor* key_cache,
+    const rel_attn_tensor* value_cache,
+    const rel_attn_tensor* block_table,
+    const rel_attn_tensor* cache_seqlens,
+    const rel_attn_tensor* cu_seqlens_q,
+    int32_t max_seqlen_q,
+    float softmax_scale,
+    int32_t causal,
+    int32_t window_left,
+    int32_t window_right,
+    int32_t rel_extent,
+    const rel_attn_tensor* rel_logits,
+    int32_t num_splits,
+    rel_attn_tensor* out,
+    rel_attn_stream stream);
+
+/*
  * rel_attn_num_splits - split-KV cap for this attention, defined by
  * inkling_fa4_num_splits (vLLM API docs, fa4_rel_attention) without its
  * Hopper branch (this library runs on sm_103 only).  Local (windowed)

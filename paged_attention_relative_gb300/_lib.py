@@ -21,8 +21,8 @@ STATUS = {0: "OK", 1: "INVALID_ARGUMENT", 2: "UNSUPPORTED", 3: "CUDA", 4: "OUT_O
 KERNELS = {0: "none", 1: "decode", 2: "prefill"}
 
 # Every function the headers declare, with its ctypes signature.
-EXPORTS = ("rel_attn_paged_varlen", "rel_attn_num_splits", "rel_attn_last_error",
-           "rel_attn_last_launch", "rel_attn_set_kernel_events", "rel_attn_device_error")
+EXPORTS = ("rel_attn_paged_varlen", "rel_attn_paged_varlen_noalloc", "rel_attn_num_splits",
+           "rel_attn_last_error", "rel_attn_last_launch", "rel_attn_set_kernel_events", "rel_attn_device_error")
 
 
 class RelAttnTensor(ctypes.Structure):
@@ -51,6 +51,8 @@ def _load() -> ctypes.CDLL:
     i32, f32 = ctypes.c_int32, ctypes.c_float
     lib.rel_attn_paged_varlen.argtypes = [P, P, P, P, P, P, i32, f32, i32, i32, i32, i32, P, i32, P, ctypes.c_void_p]
     lib.rel_attn_paged_varlen.restype = ctypes.c_int
+    lib.rel_attn_paged_varlen_noalloc.argtypes = lib.rel_attn_paged_varlen.argtypes
+    lib.rel_attn_paged_varlen_noalloc.restype = ctypes.c_int
     lib.rel_attn_num_splits.argtypes = [i32] * 6
     lib.rel_attn_num_splits.restype = i32
     lib.rel_attn_last_error.argtypes = []
@@ -114,6 +116,25 @@ def rel_attn_paged_varlen(q, key_cache, value_cache, block_table, cache_seqlens,
     st = lib.rel_attn_paged_varlen(*[_ref(d) for d in descs], int(max_seqlen_q), float(softmax_scale),
                                    int(bool(causal)), int(window_left), int(window_right), int(rel_extent),
                                    _ref(rel), int(num_splits), _ref(od), ctypes.c_void_p(stream))
+    _check(st)
+    return out
+
+
+def rel_attn_paged_varlen_noalloc(q, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_q,
+                                  max_seqlen_q, softmax_scale, causal, window_left, window_right, rel_extent,
+                                  rel_logits, num_splits, out, stream=None):
+    """The allocation-free decode entry point; ``out`` must be provided."""
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    descs = [describe(t) for t in (q, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_q)]
+    rel = describe(rel_logits) if rel_extent > 0 else None
+    od = describe(out)
+    st = lib.rel_attn_paged_varlen_noalloc(*[_ref(d) for d in descs], int(max_seqlen_q), float(softmax_scale),
+                                           int(bool(causal)), int(window_left), int(window_right),
+                                           int(rel_extent), _ref(rel), int(num_splits), _ref(od),
+                                           ctypes.c_void_p(stream))
     _check(st)
     return out
 

@@ -449,3 +449,15 @@ extern "C" rel_attn_status rel_attn_paged_varlen(
     if (e != cudaSuccess) return fail(REL_ATTN_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
     return REL_ATTN_OK;
 }
+
+namespace relattn {
+
+// Accessors for entry points defined in other files.
+void set_last_error_message(const char* msg) { t_last_error = msg; }
+
+int* device_error_word() {
+    DeviceInfo* dev = nullptr;
+    return device_info(&dev) == REL_ATTN_OK ? dev->err : nullptr;
+}
+
+}  // namespace relattn
