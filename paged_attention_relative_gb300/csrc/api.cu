@@ -339,9 +339,7 @@ extern "C" rel_attn_status rel_attn_paged_varlen(
 
     const int64_t G = H / Hk;
     const int64_t rows = (int64_t)max_seqlen_q * G;
-    if (rows > 64)
-        return fail(REL_ATTN_ERR_UNSUPPORTED, "max_seqlen_q * (H / Hk) = %lld > 64 needs the prefill kernel",
-                    (long long)rows);
+    const bool prefill = rows > 64;  // decode kernel up to 64 packed rows, tcgen05 tiles above
 
     if (check_enabled()) {
         cudaError_t e = cudaMemsetAsync(dev->check_err, 0, sizeof(int), stream);
@@ -391,7 +389,7 @@ extern "C" rel_attn_status rel_attn_paged_varlen(
     p.G = (int32_t)G;
     p.BS = (int32_t)BS;
     p.D = (int32_t)D;
-    p.max_rows = (int32_t)rows;
+    p.max_rows = (int32_t)(rows > INT32_MAX ? INT32_MAX : rows);
     p.max_seqlen_q = max_seqlen_q;
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
     p.causal = causal ? 1 : 0;
@@ -422,11 +420,11 @@ extern "C" rel_attn_status rel_attn_paged_varlen(
         p.ws_lse = p.ws_o + (size_t)splits * T * H * D;
     }
 
-    LaunchShape shape = decode_shape(p, dev->sms);
+    LaunchShape shape = prefill ? prefill_shape(p) : decode_shape(p, dev->sms);
     p.nstage = shape.nstage;
     p.nprod = shape.nprod;
     if (t_ev_begin) cudaEventRecord(t_ev_begin, stream);
-    cudaError_t e = launch_decode(p, shape, stream);
+    cudaError_t e = prefill ? launch_prefill(p, shape, stream) : launch_decode(p, shape, stream);
     if (t_ev_end) cudaEventRecord(t_ev_end, stream);
     int launches = 1;
     if (e == cudaSuccess && splits > 1) {
@@ -437,7 +435,7 @@ extern "C" rel_attn_status rel_attn_paged_varlen(
         cudaError_t e2 = cudaFreeAsync(ws, stream);
         if (e == cudaSuccess) e = e2;
     }
-    t_launch.kernel = REL_ATTN_KERNEL_DECODE;
+    t_launch.kernel = prefill ? REL_ATTN_KERNEL_PREFILL : REL_ATTN_KERNEL_DECODE;
     t_launch.num_splits = (int32_t)splits;
     t_launch.grid[0] = (int32_t)shape.grid.x;
     t_launch.grid[1] = (int32_t)shape.grid.y;

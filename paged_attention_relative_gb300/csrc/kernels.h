@@ -52,6 +52,10 @@ struct LaunchShape {
 LaunchShape decode_shape(const AttnParams& p, int num_sms);
 cudaError_t launch_decode(const AttnParams& p, const LaunchShape& shape, cudaStream_t stream);
 
+// tcgen05 prefill kernel for 128-row GQA-packed query tiles.
+LaunchShape prefill_shape(const AttnParams& p);
+cudaError_t launch_prefill(const AttnParams& p, const LaunchShape& shape, cudaStream_t stream);
+
 // LSE-weighted merge of split partials into bf16 out.
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t stream);
 
