@@ -378,6 +378,7 @@ extern "C" rel_attn_status rel_attn_paged_varlen(
     p.cu_seqlens_q = static_cast<const int32_t*>(cu_seqlens_q->data);
     p.rel = rel_extent > 0 ? rel_logits->data : nullptr;
     p.R = rel_extent;
+    p.vec_bias = (rel_extent > 0 && rel_extent % 8 == 0 && aligned(rel_logits->data, 16)) ? 1 : 0;
     p.out = out->data;
     p.o_st = out->stride[0];
     p.o_sh = out->stride[1];

@@ -35,6 +35,7 @@ struct AttnParams {
     int32_t causal, wl, wr;
     int32_t nstage;
     int32_t nprod;             // decode: producer warps
+    int32_t vec_bias;          // rel_logits rows 16-byte aligned (R % 8 == 0): staged by 16-byte copies
     uint64_t timeout_ns;
     int* err;                  // device error word (bounded-wait timeouts)
 };

@@ -8,21 +8,30 @@
 // and the bias band come first, so the running maximum settles early).
 //
 // Warp roles (256 threads):
-//   warps 0-2  producers: gather Q once and each K / V tile from the paged
-//              cache with 16-byte cp.async (one block-table lookup per key,
-//              zero-fill outside the visible range) into 128-byte-swizzled
-//              K-major tiles; after their copies land they fence the async
-//              proxy and arrive on the tile's full mbarrier.
+//   warps 0-1  Q/K/V producers: gather Q once and each K / V tile from the
+//              paged cache with 16-byte cp.async (block ids fetched once per
+//              16-key page and shared by warp shuffle; zero-fill outside the
+//              visible range) into 128-byte-swizzled tiles; after their copies
+//              land they fence the async proxy and arrive on the tile's full
+//              mbarrier.
+//   warp 2     idle.
 //   warp 3     MMA issuer (one thread) and TMEM owner: S_j = Q K_j^T into one
 //              of two TMEM buffers (M=128, N=128, K=head_dim), then
-//              O += P_{j-1} V_{j-1} (P from shared memory, V read MN-major)
-//              into a TMEM accumulator; tcgen05.commit signals completion.
+//              O += P_{j-1} V_{j-1} with P read from TMEM and V from shared
+//              memory (MN-major); tcgen05.commit signals completion.
 //   warps 4-7  softmax: thread r owns row r (TMEM lane r).  It reads S_j,
 //              applies scale, the sheared relative bias and the mask, keeps
-//              the fp32 online softmax (base 2), writes P_j as bf16, rescales
-//              its O row in TMEM when its maximum grew, and writes the output.
+//              the fp32 online softmax (base 2), writes P_j into TMEM as bf16
+//              pairs, rescales its O row when its maximum grew, and writes the
+//              output.  For key tiles that reach its bias band it prefetches,
+//              one band tile ahead, its own 272-byte window of rel_logits
+//              (16-byte aligned, the 128 distances the tile needs) into its
+//              shared-memory row with cp.async.
 // Every mbarrier wait is bounded; on timeout the kernel records the site in
 // the device error word and winds down.
+//
+// TMEM columns: S0 [0,128), S1 [128,256), O [256,256+D), P0 [384,448),
+// P1 [448,512).
 //
 // Semantics: vLLM API docs, inkling_fa4_rel_attention (paged varlen forward);
 // bias rule: prhub report on vLLM PR #48858, score_mod_rel_bias.
@@ -40,18 +49,20 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct PrefillCfg {
-    static constexpr int BN = 128;  // keys per tile (query tiles are 128 rows)
+    static constexpr int BN = 128;                  // keys per tile (query tiles are 128 rows)
     static constexpr int kDB = D / 64;              // 64-dim (128-byte) column blocks
     static constexpr int kBlk = 128 * 128;          // one 128-row x 128-byte block
     static constexpr int kTileBytes = kDB * kBlk;   // a Q, K or V tile
-    static constexpr int kPBytes = 2 * kBlk;        // P: 128 rows x 128 keys, bf16
-    static constexpr int kProdThreads = 96;         // warps 0-2
+    static constexpr int kProdThreads = 64;         // warps 0-1
     static constexpr int kMmaWarp = 3;
-    static constexpr int kStages = D == 128 ? 4 : 6;  // K/V ring slots (K even, V odd sequence numbers)
+    static constexpr int kStages = D == 128 ? 4 : 8;  // K/V ring slots (K even, V odd sequence numbers)
     static constexpr int kLag = 2;                    // copy groups in flight per producer thread
-    static constexpr int kData = kTileBytes + kStages * kTileBytes + 2 * kPBytes;
+    static constexpr int kBiasRow = 272;              // bytes per row of the staged bias window
+    static constexpr int kBiasBytes = 128 * kBiasRow;
+    static constexpr int kData = kTileBytes + kStages * kTileBytes + kBiasBytes;
     static constexpr int kTmemCols = 512;
     static constexpr int kOCol = 256;
+    static constexpr int kPCol = 384;  // + 64 * buffer
 };
 
 struct PrefillBars {
@@ -72,15 +83,19 @@ __device__ __forceinline__ bool aborted(const PrefillBars* bars) {
     return *reinterpret_cast<const volatile int*>(&bars->abort) != 0;
 }
 
-template <int D>
+__device__ __forceinline__ int floor_div8(int x) { return x >= 0 ? x >> 3 : -((-x + 7) >> 3); }
+
+// VEC: rel_logits rows are 16-byte aligned (R % 8 == 0), so bias windows are
+// staged by 16-byte copies; otherwise the bias is read per element.
+template <int D, bool VEC>
 __global__ void __launch_bounds__(256, 1) prefill_kernel(const AttnParams p) {
     using C = PrefillCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem;
     uint8_t* sKV = smem + C::kTileBytes;
-    uint8_t* sP = sKV + C::kStages * C::kTileBytes;
-    PrefillBars* bars = reinterpret_cast<PrefillBars*>(sP + 2 * C::kPBytes);
+    uint8_t* sBias = sKV + C::kStages * C::kTileBytes;
+    PrefillBars* bars = reinterpret_cast<PrefillBars*>(sBias + C::kBiasBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.G, TPT = 128 / G;
@@ -97,6 +112,7 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const AttnParams p) {
     const int n_rows = (i1 - i0) * G;
     const int off = sk - sq;
     const int pos_min = i0 + off, pos_max = i1 - 1 + off;
+    const int R = p.R;
 
     // Keys any row of the tile may see, as 128-key tiles, split contiguously.
     int hi = sk;
@@ -117,6 +133,9 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const AttnParams p) {
     }
     const int n_it = t_end - t_begin;
     auto key_block = [&](int jj) { return kb_first + t_end - 1 - jj; };  // last tile first
+    // Does key tile [j0, j0+128) reach the bias band 0 <= pos - j < R of some row?
+    constexpr bool vec_bias = VEC;
+    auto band_tile = [&](int j0) { return R > 0 && pos_max - j0 >= 0 && pos_min - (j0 + C::BN - 1) < R; };
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, C::kProdThreads);
@@ -147,16 +166,27 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const AttnParams p) {
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp < 3) {
-        // ------------------------------------------------------------ producers
-        const int pt = threadIdx.x;
+    if (warp < 2) {
+        // ------------------------------------------------------ Q/K/V producers
+        // Warp w copies rows [64w, 64w + 64) of every tile; one warp-wide copy
+        // covers kRows rows (kChunks lanes per 256- or 128-byte row).
+        constexpr int kChunks = D / 8;
+        constexpr int kRows = 32 / kChunks;
+        constexpr int kCopies = 64 / kRows;
+        const int lrow = lane / kChunks, lchunk = lane % kChunks;
         const uint16_t* qg = reinterpret_cast<const uint16_t*>(p.q);
         const uint16_t* kc = reinterpret_cast<const uint16_t*>(p.k_cache);
         const uint16_t* vc = reinterpret_cast<const uint16_t*>(p.v_cache);
         const int32_t* bt = p.block_table + (size_t)b * p.bt_stride;
         const uint64_t pol_first = l2_policy_evict_first();
         const uint64_t pol_last = l2_policy_evict_last();
-        constexpr int kChunks = C::kDB * 8;  // 16-byte chunks per 128-row tile row
+        const uint32_t col_off = (lchunk >> 3) * C::kBlk;
+        // K/V copies: lane_off walks this lane's rows inside a page; dst_lane is
+        // the lane's swizzled position in row 64*warp + lrow of a tile.
+        const long long lane_off = (long long)lrow * p.c_s1 + lchunk * 8;
+        const long long row_step = (long long)kRows * p.c_s1;
+        const uint32_t cx = (uint32_t)((lchunk & 7) ^ lrow);
+        const uint32_t dst_lane = col_off + (64 * warp + lrow) * 128;
         int issued = 0, done = 0;
         auto complete = [&](int k) {  // copy group k of this thread has landed
             fence_proxy_async_smem();
@@ -165,39 +195,58 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const AttnParams p) {
             else
                 mbar_arrive(&bars->kv_full[(k - 1) % C::kStages]);
         };
-        // Q tile (group 0)
-        for (int idx = pt; idx < 128 * kChunks; idx += C::kProdThreads) {
-            const int r = idx / kChunks, c = idx % kChunks;
+#pragma unroll 4
+        for (int k = 0; k < kCopies; ++k) {  // Q tile (group 0)
+            const int r = 64 * warp + k * kRows + lrow;
             const bool valid = r < n_rows;
             const int tok = i0 + r / G, hh = r % G;
-            const uint16_t* src = qg + (size_t)(q0 + tok) * p.q_st + (size_t)(g * G + hh) * p.q_sh + c * 8;
-            const uint32_t dst = smem_u32(sQ) + (c >> 3) * C::kBlk + sw128_offset(r, c & 7);
-            cp_async_16(dst, valid ? src : qg, valid ? 16u : 0u, pol_first);
+            const uint16_t* src = qg + (size_t)(q0 + tok) * p.q_st + (size_t)(g * G + hh) * p.q_sh + lchunk * 8;
+            cp_async_16(smem_u32(sQ) + col_off + sw128_offset(r, lchunk & 7), valid ? src : qg, valid ? 16u : 0u,
+                        pol_first);
         }
         cp_async_commit();
         ++issued;
         for (int seq = 0; seq < 2 * n_it; ++seq) {
             const int slot = seq % C::kStages;
             const int round = seq / C::kStages;
-            if (!mbar_wait(&bars->kv_empty[slot], (round & 1) ^ 1, p.timeout_ns, kSitePrefillKEmpty, p.err)) {
-                bars->abort = 1;
-                break;
+            // Never block on a full ring while holding copies whose landing has
+            // not been signalled: the consumer may be waiting for exactly those.
+            if (!mbar_try_wait(&bars->kv_empty[slot], (round & 1) ^ 1)) {
+                while (done < issued) {
+                    cp_async_wait(issued - done - 1);
+                    complete(done++);
+                }
+                if (!mbar_wait(&bars->kv_empty[slot], (round & 1) ^ 1, p.timeout_ns, kSitePrefillKEmpty, p.err))
+                    bars->abort = 1;
             }
-            if (aborted(bars)) break;
-            const int j0 = key_block(seq >> 1) * C::BN;
+            if (__any_sync(0xffffffffu, aborted(bars))) break;
+            const int j0 = key_block(seq >> 1) * C::BN + 64 * warp;  // this warp's first key
             const uint16_t* cache = (seq & 1) ? vc : kc;
-            const uint32_t dst0 = smem_u32(sKV + slot * C::kTileBytes);
-            for (int idx = pt; idx < 128 * kChunks; idx += C::kProdThreads) {
-                const int r = idx / kChunks, c = idx % kChunks;
-                const int j = j0 + r;
-                const bool valid = j >= lo && j < hi;
-                const int n = j / p.BS;
-                int blk = valid ? __ldg(bt + n) : 0;
-                blk = min(max(blk, 0), p.NB - 1);  // an out-of-range id stays inside the cache
-                const uint16_t* src =
-                    cache + (size_t)blk * p.c_s0 + (size_t)(j - n * p.BS) * p.c_s1 + (size_t)g * p.c_s2 + c * 8;
-                const uint32_t dst = dst0 + (c >> 3) * C::kBlk + sw128_offset(r, c & 7);
-                cp_async_16(dst, valid ? src : cache, valid ? 16u : 0u, pol_last);
+            // Element offset of each of this warp's four 16-key pages (lanes 0-3).
+            long long my_page = 0;
+            if (lane < 4) {
+                const int jg = j0 + 16 * lane;
+                if (jg + 15 >= lo && jg < hi) {
+                    const int blk = min(max(__ldg(bt + jg / p.BS), 0), p.NB - 1);
+                    my_page = (long long)blk * p.c_s0 + (long long)(jg % p.BS) * p.c_s1 + (long long)g * p.c_s2;
+                }
+            }
+            const bool span_full = j0 >= lo && j0 + 64 <= hi;  // every key of the warp's 64 is visible
+            const uint32_t dst_tile = smem_u32(sKV + slot * C::kTileBytes) + dst_lane;
+#pragma unroll
+            for (int pg = 0; pg < 4; ++pg) {
+                const long long poff = __shfl_sync(0xffffffffu, my_page, pg);
+                const uint16_t* src = cache + poff + lane_off;
+#pragma unroll
+                for (int kk = 0; kk < 16 / kRows; ++kk) {
+                    const int row = pg * 16 + kk * kRows;  // + lrow, within the warp's 64 rows
+                    const bool valid = span_full || (j0 + row + lrow >= lo && j0 + row + lrow < hi);
+                    // row & 7 == (kk * kRows) & 7 | lrow, so the swizzle is a per-lane constant
+                    // XOR a compile-time one.
+                    const uint32_t dst = dst_tile + row * 128 + ((cx ^ ((kk * kRows) & 7)) << 4);
+                    cp_async_16(dst, valid ? src : cache, valid ? 16u : 0u, pol_last);
+                    src += row_step;
+                }
             }
             cp_async_commit();
             ++issued;
@@ -211,11 +260,11 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const AttnParams p) {
             complete(done++);
         }
     } else if (warp == C::kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------ MMA issuer
         if (lane == 0 && n_it > 0) {
             constexpr uint32_t idS = umma_idesc_bf16(128, C::BN, false);
             constexpr uint32_t idPV = umma_idesc_bf16(128, D, true);
-            const uint32_t aQ = smem_u32(sQ), aKV = smem_u32(sKV), aP = smem_u32(sP);
+            const uint32_t aQ = smem_u32(sQ), aKV = smem_u32(sKV);
             bool ok = mbar_wait(&bars->q_full, 0, p.timeout_ns, kSitePrefillLoadQ, p.err);
             auto issue_pv = [&](int t) {
                 const int pb = t & 1;
@@ -226,13 +275,12 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const AttnParams p) {
                                      p.err);
                 if (!ok) return;
                 tc_fence_after();
-                const uint32_t pbase = aP + pb * C::kPBytes;
                 const uint32_t vbase = aKV + slot * C::kTileBytes;
+                const uint32_t pcol = tmem + C::kPCol + 64 * pb;
 #pragma unroll
                 for (int kk = 0; kk < C::BN / 16; ++kk) {
-                    const uint64_t da = umma_desc_sw128(pbase + (kk >> 2) * C::kBlk + (kk & 3) * 32, 16, 1024);
                     const uint64_t db = umma_desc_sw128(vbase + kk * 16 * 128, C::kBlk, 1024);
-                    umma_bf16(tmem + C::kOCol, da, db, idPV, (t > 0 || kk > 0) ? 1u : 0u);
+                    umma_bf16_tmem_a(tmem + C::kOCol, pcol + kk * 8, db, idPV, (t > 0 || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(&bars->o_done);
                 umma_commit(&bars->kv_empty[slot]);
@@ -266,94 +314,150 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const AttnParams p) {
             if (!ok) bars->abort = 1;
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------------------------ softmax
+    } else if (warp >= 4) {
+        // ------------------------------------------------------ softmax
         const int r = threadIdx.x - 128;  // row == TMEM lane
         const bool valid = r < n_rows;
         const int tok = i0 + (valid ? r / G : 0);
         const int hh = valid ? r % G : 0;
         const int t = q0 + tok, h = g * G + hh;
         const int pos = tok + off;
-        const uint16_t* relrow =
-            p.R > 0 ? reinterpret_cast<const uint16_t*>(p.rel) + ((size_t)t * p.H + h) * p.R : nullptr;
+        // Keys this row may see: [klo, khi).
+        int khi = sk;
+        if (p.causal) khi = min(khi, pos + 1);
+        if (p.wr >= 0) khi = min(khi, pos + p.wr + 1);
+        int klo = 0;
+        if (p.wl >= 0) klo = max(0, pos - p.wl);
+        const uint16_t* relg = reinterpret_cast<const uint16_t*>(p.rel);
+        const size_t rel_row = ((size_t)t * p.H + h) * (size_t)R;
+        const uint32_t bias_row_s = smem_u32(sBias + r * C::kBiasRow);
+        const uint32_t bias_dst = smem_u32(sBias + r * C::kBiasRow);
+        const uint64_t pol_first = l2_policy_evict_first();
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const float sl2 = p.scale_log2;
-        const int R = p.R, wl = p.wl, wr = p.wr, causal = p.causal;
+        const bool pos_scale = sl2 > 0.f;
         float m_run = -CUDART_INF_F, l_run = 0.f;
-        const uint32_t aP = smem_u32(sP);
+
+        // Band tiles form one contiguous run of jj; prefetch this row's window
+        // for the first one, then for each next one while the current is used.
+        auto prefetch_bias = [&](int j0n) {
+            const int qa = floor_div8(pos - j0n - (C::BN - 1));
+#pragma unroll
+            for (int i = 0; i < C::kBiasRow / 16; ++i) {
+                const int q = qa + i;
+                const bool ok = valid && q >= 0 && 8 * q + 8 <= R;
+                cp_async_16(bias_dst + 16 * i, ok ? relg + rel_row + 8 * q : relg, ok ? 16u : 0u, pol_first);
+            }
+            cp_async_commit();
+        };
+        if (vec_bias) {
+            for (int jj = 0; jj < n_it; ++jj)
+                if (band_tile(key_block(jj) * C::BN)) {
+                    prefetch_bias(key_block(jj) * C::BN);
+                    break;
+                }
+        }
 
         for (int jj = 0; jj < n_it; ++jj) {
             const int sb = jj & 1;
             const int j0 = key_block(jj) * C::BN;
-            if (!mbar_wait(&bars->s_full[sb], (jj >> 1) & 1, p.timeout_ns, kSitePrefillSFull, p.err)) {
+            const bool band = band_tile(j0);
+            if (!mbar_wait(&bars->s_full[sb], (jj >> 1) & 1, p.timeout_ns, kSitePrefillSFull, p.err))
                 bars->abort = 1;
-            }
             if (__any_sync(0xffffffffu, aborted(bars))) break;  // warp-uniform: TMEM access is collective
             tc_fence_after();
             float s[C::BN];
-#pragma unroll
-            for (int c = 0; c < C::BN / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(lane_base + sb * C::BN + c * 32, v);
+            {
+                uint32_t v0[32], v1[32], v2[32], v3[32];
+                tmem_ld32(lane_base + sb * C::BN + 0, v0);
+                tmem_ld32(lane_base + sb * C::BN + 32, v1);
+                tmem_ld32(lane_base + sb * C::BN + 64, v2);
+                tmem_ld32(lane_base + sb * C::BN + 96, v3);
                 tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(v[e]);
+                for (int e = 0; e < 32; ++e) {
+                    s[e] = __uint_as_float(v0[e]);
+                    s[32 + e] = __uint_as_float(v1[e]);
+                    s[64 + e] = __uint_as_float(v2[e]);
+                    s[96 + e] = __uint_as_float(v3[e]);
+                }
             }
             tc_fence_before();
             mbar_arrive(&bars->s_empty[sb]);
 
             // Scale, sheared bias, mask.  Fast path: the whole key tile is
-            // visible to this row and out of its bias band.
-            const bool all_visible = !valid || ((j0 + C::BN <= sk) && (!causal || pos - (j0 + C::BN - 1) >= 0) &&
-                                                (wl < 0 || pos - j0 <= wl) && (wr < 0 || pos - (j0 + C::BN - 1) >= -wr));
-            const bool no_bias = !valid || R == 0 || pos - (j0 + C::BN - 1) >= R || pos - j0 < 0;
-            float mx = -CUDART_INF_F;
-            if (all_visible && no_bias) {
+            // visible to this row and outside its bias band; then s keeps the
+            // raw q.k and the scale is folded into the exponent below.
+            const bool row_full = !valid || (j0 >= klo && j0 + C::BN <= khi);
+            const bool row_band = valid && band && j0 + C::BN - 1 >= pos - R + 1 && j0 <= pos;
+            const bool raw = row_full && !row_band && pos_scale;
+            float mk[8];
 #pragma unroll
-                for (int k = 0; k < C::BN; ++k) {
-                    s[k] *= sl2;
-                    mx = fmaxf(mx, s[k]);
-                }
+            for (int i = 0; i < 8; ++i) mk[i] = -CUDART_INF_F;
+            if (raw) {
+#pragma unroll
+                for (int k = 0; k < C::BN; ++k) mk[k & 7] = fmaxf(mk[k & 7], s[k]);
             } else {
+                if (band && vec_bias) cp_async_wait(0);  // this row's window has landed
+                // Window offset of distance d = pos - j0 - k is o + 127 - k;
+                // outside [0, R) the window holds zeros.
+                const int o = (pos - j0 - (C::BN - 1)) - 8 * floor_div8(pos - j0 - (C::BN - 1));
 #pragma unroll
                 for (int k = 0; k < C::BN; ++k) {
                     const int j = j0 + k;
-                    const int d = pos - j;
-                    bool allowed = j < sk;
-                    if (causal) allowed = allowed && d >= 0;
-                    if (wl >= 0) allowed = allowed && d <= wl;
-                    if (wr >= 0) allowed = allowed && d >= -wr;
                     float bias = 0.f;
-                    if (allowed && d >= 0 && d < R) bias = bf16_bits_to_f32(__ldg(relrow + d));
-                    s[k] = allowed ? fmaf(s[k], sl2, bias * kLog2e) : -CUDART_INF_F;
-                    mx = fmaxf(mx, s[k]);
+                    if (row_band) {
+                        if constexpr (VEC) {
+                            bias = bf16_bits_to_f32(lds_u16(bias_row_s + 2 * (o + (C::BN - 1) - k)));
+                        } else {
+                            const int d = pos - j;
+                            if (d >= 0 && d < R) bias = bf16_bits_to_f32(__ldg(relg + rel_row + d));
+                        }
+                    }
+                    float v = fmaf(s[k], sl2, bias * kLog2e);
+                    if (!row_full && !(j >= klo && j < khi)) v = -CUDART_INF_F;
+                    s[k] = v;
+                    mk[k & 7] = fmaxf(mk[k & 7], v);
                 }
             }
+            if (band && vec_bias && jj + 1 < n_it && band_tile(key_block(jj + 1) * C::BN))
+                prefetch_bias(key_block(jj + 1) * C::BN);
+            float mx = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])),
+                             fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
+            if (raw) mx *= sl2;
             const float m_new = fmaxf(m_run, mx);
             const float mu = m_new == -CUDART_INF_F ? 0.f : m_new;
             const bool grow = m_run != -CUDART_INF_F && m_new > m_run;
             const float alpha = grow ? ex2(m_run - m_new) : 1.f;
 
-            // P_j into shared buffer jj % 2 once PV_{j-2} has read it.
+            // P_j into TMEM buffer jj % 2 once PV_{j-2} has read it.
             if (!mbar_wait(&bars->p_free[sb], ((jj >> 1) & 1) ^ 1, p.timeout_ns, kSitePrefillPFull, p.err))
                 bars->abort = 1;
-            float rs = 0.f;
-            const uint32_t prow = aP + sb * C::kPBytes;
+            float rs[8];
 #pragma unroll
-            for (int c = 0; c < C::BN / 8; ++c) {
-                uint32_t w[4];
+            for (int i = 0; i < 8; ++i) rs[i] = 0.f;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float a = ex2(s[c * 8 + 2 * e] - mu), bq = ex2(s[c * 8 + 2 * e + 1] - mu);
-                    rs += a + bq;
+            for (int c = 0; c < 2; ++c) {
+                uint32_t w[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int k = c * 64 + 2 * e;
+                    float a, bq;
+                    if (raw) {
+                        a = ex2(fmaf(s[k], sl2, -mu));
+                        bq = ex2(fmaf(s[k + 1], sl2, -mu));
+                    } else {
+                        a = ex2(s[k] - mu);
+                        bq = ex2(s[k + 1] - mu);
+                    }
+                    rs[k & 7] += a;
+                    rs[(k + 1) & 7] += bq;
                     w[e] = pack_bf16(a, bq);
                 }
-                const uint32_t addr = prow + (c >> 3) * C::kBlk + sw128_offset(r, c & 7);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-                             "r"(w[3])
-                             : "memory");
+                tmem_st32(lane_base + C::kPCol + 64 * sb + 32 * c, w);
             }
-            l_run = l_run * alpha + rs;
+            const float rsum = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+            l_run = l_run * alpha + rsum;
             m_run = m_new;
 
             // Rescale the O row when its maximum grew (warp-collective TMEM access).
@@ -369,12 +473,12 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const AttnParams p) {
                     for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
                     tmem_st32(lane_base + C::kOCol + c * 32, v);
                 }
-                tmem_wait_st();
             }
-            fence_proxy_async_smem();  // P stores -> visible to the tensor core
+            tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&bars->p_full[sb]);
         }
+        cp_async_wait(0);
 
         // Epilogue: O / l.
         const bool have = __all_sync(0xffffffffu, n_it > 0 && !aborted(bars));
@@ -438,9 +542,9 @@ int prefill_smem_bytes() {
     return 1024 + PrefillCfg<D>::kData + (int)sizeof(PrefillBars);
 }
 
-template <int D>
+template <int D, bool VEC>
 cudaError_t launch_t(const AttnParams& p, const LaunchShape& s, cudaStream_t stream) {
-    auto kern = prefill_kernel<D>;
+    auto kern = prefill_kernel<D, VEC>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, s.smem);
     if (e != cudaSuccess) return e;
     kern<<<s.grid, s.block, s.smem, stream>>>(p);
@@ -461,8 +565,9 @@ LaunchShape prefill_shape(const AttnParams& p) {
 }
 
 cudaError_t launch_prefill(const AttnParams& p, const LaunchShape& s, cudaStream_t stream) {
-    if (p.D == 128) return launch_t<128>(p, s, stream);
-    if (p.D == 64) return launch_t<64>(p, s, stream);
+    const bool vec = p.vec_bias != 0;
+    if (p.D == 128) return vec ? launch_t<128, true>(p, s, stream) : launch_t<128, false>(p, s, stream);
+    if (p.D == 64) return vec ? launch_t<64, true>(p, s, stream) : launch_t<64, false>(p, s, stream);
     return cudaErrorInvalidValue;
 }
 
