@@ -7,31 +7,35 @@
 // 128-key tiles, processed from the last to the first (the causal diagonal
 // and the bias band come first, so the running maximum settles early).
 //
-// Warp roles (256 threads):
-//   warps 0-1  Q/K/V producers: gather Q once and each K / V tile from the
-//              paged cache with 16-byte cp.async (block ids fetched once per
-//              16-key page and shared by warp shuffle; zero-fill outside the
-//              visible range) into 128-byte-swizzled tiles; after their copies
-//              land they fence the async proxy and arrive on the tile's full
-//              mbarrier.
-//   warp 2     idle.
+// Warp roles (384 threads):
+//   warps 0-2  Q/K/V producers: warp w gathers the 16-key pages w, w+3, w+6
+//              of Q (once) and of each K / V tile from the paged cache with
+//              16-byte cp.async (one block-table lookup per page, zero-fill
+//              outside the visible range) into 128-byte-swizzled tiles; after
+//              their copies land they fence the async proxy and arrive on the
+//              tile's full mbarrier.
 //   warp 3     MMA issuer (one thread) and TMEM owner: S_j = Q K_j^T into one
 //              of two TMEM buffers (M=128, N=128, K=head_dim), then
 //              O += P_{j-1} V_{j-1} with P read from TMEM and V from shared
 //              memory (MN-major); tcgen05.commit signals completion.
-//   warps 4-7  softmax: thread r owns row r (TMEM lane r).  It reads S_j,
-//              applies scale, the sheared relative bias and the mask, keeps
-//              the fp32 online softmax (base 2), writes P_j into TMEM as bf16
-//              pairs, rescales its O row when its maximum grew, and writes the
-//              output.  For key tiles that reach its bias band it prefetches,
-//              one band tile ahead, its own 272-byte window of rel_logits
-//              (16-byte aligned, the 128 distances the tile needs) into its
-//              shared-memory row with cp.async.
+//   warps 4-11 softmax: warps 4-7 take keys [0, 64) of every tile and warps
+//              8-11 keys [64, 128); warp w reads TMEM lanes 32*(w%4).. so
+//              thread (w, lane) owns half of row 32*(w%4) + lane.  Per tile it
+//              reads its half of S_j, applies scale, the sheared relative bias
+//              and the mask, exchanges the half-row maximum with its partner
+//              through shared memory (one named barrier per tile), keeps the
+//              fp32 online softmax (base 2), writes its half of P_j into TMEM
+//              as bf16 pairs, rescales its half of the O row when the row
+//              maximum grew, and writes its half of the output.  For key tiles
+//              that reach the row's bias band it prefetches, one band tile
+//              ahead, its 144-byte window of rel_logits (16-byte aligned, the
+//              64 distances its half needs) into shared memory with cp.async.
 // Every mbarrier wait is bounded; on timeout the kernel records the site in
 // the device error word and winds down.
 //
 // TMEM columns: S0 [0,128), S1 [128,256), O [256,256+D), P0 [384,448),
-// P1 [448,512).
+// P1 [448,512); within S and P the first half of the columns holds keys
+// [0, 64) of the tile.
 //
 // Semantics: vLLM API docs, inkling_fa4_rel_attention (paged varlen forward);
 // bias rule: prhub report on vLLM PR #48858, score_mod_rel_bias.
@@ -53,13 +57,17 @@ struct PrefillCfg {
     static constexpr int kDB = D / 64;              // 64-dim (128-byte) column blocks
     static constexpr int kBlk = 128 * 128;          // one 128-row x 128-byte block
     static constexpr int kTileBytes = kDB * kBlk;   // a Q, K or V tile
-    static constexpr int kProdThreads = 64;         // warps 0-1
+    static constexpr int kProdWarps = 3;
+    static constexpr int kProdThreads = 96;         // warps 0-2
     static constexpr int kMmaWarp = 3;
+    static constexpr int kSoftThreads = 256;        // warps 4-11
+    static constexpr int kThreads = 384;
     static constexpr int kStages = D == 128 ? 4 : 8;  // K/V ring slots (K even, V odd sequence numbers)
     static constexpr int kLag = 2;                    // copy groups in flight per producer thread
-    static constexpr int kBiasRow = 272;              // bytes per row of the staged bias window
-    static constexpr int kBiasBytes = 128 * kBiasRow;
-    static constexpr int kData = kTileBytes + kStages * kTileBytes + kBiasBytes;
+    static constexpr int kBiasRow = 144;              // bytes of one half-row bias window (9 chunks)
+    static constexpr int kBiasBytes = 2 * 128 * kBiasRow;
+    static constexpr int kXchBytes = 3 * 2 * 128 * 4;  // half-row maxima (2 buffers), half-row sums
+    static constexpr int kData = kTileBytes + kStages * kTileBytes + kBiasBytes + kXchBytes;
     static constexpr int kTmemCols = 512;
     static constexpr int kOCol = 256;
     static constexpr int kPCol = 384;  // + 64 * buffer
@@ -88,14 +96,15 @@ __device__ __forceinline__ int floor_div8(int x) { return x >= 0 ? x >> 3 : -((-
 // VEC: rel_logits rows are 16-byte aligned (R % 8 == 0), so bias windows are
 // staged by 16-byte copies; otherwise the bias is read per element.
 template <int D, bool VEC>
-__global__ void __launch_bounds__(256, 1) prefill_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(384, 1) prefill_kernel(const AttnParams p) {
     using C = PrefillCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem;
     uint8_t* sKV = smem + C::kTileBytes;
     uint8_t* sBias = sKV + C::kStages * C::kTileBytes;
-    PrefillBars* bars = reinterpret_cast<PrefillBars*>(sBias + C::kBiasBytes);
+    float* sXch = reinterpret_cast<float*>(sBias + C::kBiasBytes);  // [3 bufs][2 halves][128 rows]
+    PrefillBars* bars = reinterpret_cast<PrefillBars*>(sBias + C::kBiasBytes + C::kXchBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.G, TPT = 128 / G;
@@ -145,8 +154,8 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const AttnParams p) {
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->s_full[i], 1);
-            mbar_init(&bars->s_empty[i], 128);
-            mbar_init(&bars->p_full[i], 128);
+            mbar_init(&bars->s_empty[i], C::kSoftThreads);
+            mbar_init(&bars->p_full[i], C::kSoftThreads);
             mbar_init(&bars->p_free[i], 1);
         }
         mbar_init(&bars->o_done, 1);
@@ -166,13 +175,13 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const AttnParams p) {
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp < 2) {
+    if (warp < C::kProdWarps) {
         // ------------------------------------------------------ Q/K/V producers
-        // Warp w copies rows [64w, 64w + 64) of every tile; one warp-wide copy
-        // covers kRows rows (kChunks lanes per 256- or 128-byte row).
+        // Warp w copies the 16-row pages w, w+3, w+6 of every tile; one
+        // warp-wide copy covers kRows rows (kChunks lanes per 256- or 128-byte row).
         constexpr int kChunks = D / 8;
         constexpr int kRows = 32 / kChunks;
-        constexpr int kCopies = 64 / kRows;
+        constexpr int kPerPage = 16 / kRows;
         const int lrow = lane / kChunks, lchunk = lane % kChunks;
         const uint16_t* qg = reinterpret_cast<const uint16_t*>(p.q);
         const uint16_t* kc = reinterpret_cast<const uint16_t*>(p.k_cache);
@@ -181,12 +190,13 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const AttnParams p) {
         const uint64_t pol_first = l2_policy_evict_first();
         const uint64_t pol_last = l2_policy_evict_last();
         const uint32_t col_off = (lchunk >> 3) * C::kBlk;
-        // K/V copies: lane_off walks this lane's rows inside a page; dst_lane is
-        // the lane's swizzled position in row 64*warp + lrow of a tile.
+        // lane_off walks this lane's rows inside a page; within a page row
+        // (16*pg + kk*kRows + lrow) & 7 == ((kk*kRows) & 7) | lrow, so the
+        // swizzle is the per-lane constant cx XOR a compile-time one.
         const long long lane_off = (long long)lrow * p.c_s1 + lchunk * 8;
         const long long row_step = (long long)kRows * p.c_s1;
         const uint32_t cx = (uint32_t)((lchunk & 7) ^ lrow);
-        const uint32_t dst_lane = col_off + (64 * warp + lrow) * 128;
+        const uint32_t dst_lane = col_off + lrow * 128 + 0u;
         int issued = 0, done = 0;
         auto complete = [&](int k) {  // copy group k of this thread has landed
             fence_proxy_async_smem();
@@ -195,14 +205,17 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const AttnParams p) {
             else
                 mbar_arrive(&bars->kv_full[(k - 1) % C::kStages]);
         };
-#pragma unroll 4
-        for (int k = 0; k < kCopies; ++k) {  // Q tile (group 0)
-            const int r = 64 * warp + k * kRows + lrow;
-            const bool valid = r < n_rows;
-            const int tok = i0 + r / G, hh = r % G;
-            const uint16_t* src = qg + (size_t)(q0 + tok) * p.q_st + (size_t)(g * G + hh) * p.q_sh + lchunk * 8;
-            cp_async_16(smem_u32(sQ) + col_off + sw128_offset(r, lchunk & 7), valid ? src : qg, valid ? 16u : 0u,
-                        pol_first);
+        for (int pg = warp; pg < 8; pg += C::kProdWarps) {  // Q tile (group 0)
+#pragma unroll
+            for (int kk = 0; kk < kPerPage; ++kk) {
+                const int r = 16 * pg + kk * kRows + lrow;
+                const bool valid = r < n_rows;
+                const int tok = i0 + r / G, hh = r % G;
+                const uint16_t* src = qg + (size_t)(q0 + tok) * p.q_st + (size_t)(g * G + hh) * p.q_sh + lchunk * 8;
+                const uint32_t dst =
+                    smem_u32(sQ) + dst_lane + (16 * pg + kk * kRows) * 128 + ((cx ^ ((kk * kRows) & 7)) << 4);
+                cp_async_16(dst, valid ? src : qg, valid ? 16u : 0u, pol_first);
+            }
         }
         cp_async_commit();
         ++issued;
@@ -220,30 +233,24 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const AttnParams p) {
                     bars->abort = 1;
             }
             if (__any_sync(0xffffffffu, aborted(bars))) break;
-            const int j0 = key_block(seq >> 1) * C::BN + 64 * warp;  // this warp's first key
+            const int j0 = key_block(seq >> 1) * C::BN;
             const uint16_t* cache = (seq & 1) ? vc : kc;
-            // Element offset of each of this warp's four 16-key pages (lanes 0-3).
-            long long my_page = 0;
-            if (lane < 4) {
-                const int jg = j0 + 16 * lane;
-                if (jg + 15 >= lo && jg < hi) {
-                    const int blk = min(max(__ldg(bt + jg / p.BS), 0), p.NB - 1);
-                    my_page = (long long)blk * p.c_s0 + (long long)(jg % p.BS) * p.c_s1 + (long long)g * p.c_s2;
-                }
-            }
-            const bool span_full = j0 >= lo && j0 + 64 <= hi;  // every key of the warp's 64 is visible
             const uint32_t dst_tile = smem_u32(sKV + slot * C::kTileBytes) + dst_lane;
-#pragma unroll
-            for (int pg = 0; pg < 4; ++pg) {
-                const long long poff = __shfl_sync(0xffffffffu, my_page, pg);
+            for (int pg = warp; pg < 8; pg += C::kProdWarps) {
+                const int jg = j0 + 16 * pg;
+                long long poff = 0;
+                if (lane == 0 && jg + 15 >= lo && jg < hi) {
+                    const int blk = min(max(__ldg(bt + jg / p.BS), 0), p.NB - 1);
+                    poff = (long long)blk * p.c_s0 + (long long)(jg % p.BS) * p.c_s1 + (long long)g * p.c_s2;
+                }
+                poff = __shfl_sync(0xffffffffu, poff, 0);
+                const bool page_full = jg >= lo && jg + 16 <= hi;
                 const uint16_t* src = cache + poff + lane_off;
 #pragma unroll
-                for (int kk = 0; kk < 16 / kRows; ++kk) {
-                    const int row = pg * 16 + kk * kRows;  // + lrow, within the warp's 64 rows
-                    const bool valid = span_full || (j0 + row + lrow >= lo && j0 + row + lrow < hi);
-                    // row & 7 == (kk * kRows) & 7 | lrow, so the swizzle is a per-lane constant
-                    // XOR a compile-time one.
-                    const uint32_t dst = dst_tile + row * 128 + ((cx ^ ((kk * kRows) & 7)) << 4);
+                for (int kk = 0; kk < kPerPage; ++kk) {
+                    const int row = kk * kRows + lrow;  // key jg + row
+                    const bool valid = page_full || (jg + row >= lo && jg + row < hi);
+                    const uint32_t dst = dst_tile + (16 * pg + kk * kRows) * 128 + ((cx ^ ((kk * kRows) & 7)) << 4);
                     cp_async_16(dst, valid ? src : cache, valid ? 16u : 0u, pol_last);
                     src += row_step;
                 }
@@ -316,7 +323,8 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const AttnParams p) {
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------------ softmax
-        const int r = threadIdx.x - 128;  // row == TMEM lane
+        const int half = (warp - 4) >> 2;  // keys [64*half, 64*half + 64) of each tile
+        const int r = (warp & 3) * 32 + lane;  // row == TMEM lane
         const bool valid = r < n_rows;
         const int tok = i0 + (valid ? r / G : 0);
         const int hh = valid ? r % G : 0;
@@ -330,18 +338,22 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const AttnParams p) {
         if (p.wl >= 0) klo = max(0, pos - p.wl);
         const uint16_t* relg = reinterpret_cast<const uint16_t*>(p.rel);
         const size_t rel_row = ((size_t)t * p.H + h) * (size_t)R;
-        const uint32_t bias_row_s = smem_u32(sBias + r * C::kBiasRow);
-        const uint32_t bias_dst = smem_u32(sBias + r * C::kBiasRow);
+        uint8_t* my_bias = sBias + (half * 128 + r) * C::kBiasRow;
+        const uint16_t* bias_row = reinterpret_cast<const uint16_t*>(my_bias);
+        const uint32_t bias_dst = smem_u32(my_bias);
         const uint64_t pol_first = l2_policy_evict_first();
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const float sl2 = p.scale_log2;
         const bool pos_scale = sl2 > 0.f;
-        float m_run = -CUDART_INF_F, l_run = 0.f;
+        const int kh = 64 * half;  // first key of this half within a tile
+        float m_run = -CUDART_INF_F, l_half = 0.f;
+        bool any_abort = false;
 
-        // Band tiles form one contiguous run of jj; prefetch this row's window
-        // for the first one, then for each next one while the current is used.
+        // Band tiles form one contiguous run of jj; prefetch this half-row's
+        // window for the first one, then for each next one while the current
+        // one is in use.  Distance of key k (in the half) is d_lo + 63 - k.
         auto prefetch_bias = [&](int j0n) {
-            const int qa = floor_div8(pos - j0n - (C::BN - 1));
+            const int qa = floor_div8(pos - j0n - kh - 63);
 #pragma unroll
             for (int i = 0; i < C::kBiasRow / 16; ++i) {
                 const int q = qa + i;
@@ -361,87 +373,92 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const AttnParams p) {
         for (int jj = 0; jj < n_it; ++jj) {
             const int sb = jj & 1;
             const int j0 = key_block(jj) * C::BN;
+            const int jh = j0 + kh;  // first key of this half
             const bool band = band_tile(j0);
-            if (!mbar_wait(&bars->s_full[sb], (jj >> 1) & 1, p.timeout_ns, kSitePrefillSFull, p.err))
-                bars->abort = 1;
-            if (__any_sync(0xffffffffu, aborted(bars))) break;  // warp-uniform: TMEM access is collective
-            tc_fence_after();
-            float s[C::BN];
-            {
-                uint32_t v0[32], v1[32], v2[32], v3[32];
-                tmem_ld32(lane_base + sb * C::BN + 0, v0);
-                tmem_ld32(lane_base + sb * C::BN + 32, v1);
-                tmem_ld32(lane_base + sb * C::BN + 64, v2);
-                tmem_ld32(lane_base + sb * C::BN + 96, v3);
-                tmem_wait_ld();
+            bool my_abort = !mbar_wait(&bars->s_full[sb], (jj >> 1) & 1, p.timeout_ns, kSitePrefillSFull, p.err);
+            my_abort = __any_sync(0xffffffffu, my_abort || aborted(bars));
+            float s[64];
+            float mx = -CUDART_INF_F;
+            bool raw = false;
+            if (!my_abort) {
+                tc_fence_after();
+                {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld32(lane_base + sb * C::BN + kh, v0);
+                    tmem_ld32(lane_base + sb * C::BN + kh + 32, v1);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    s[e] = __uint_as_float(v0[e]);
-                    s[32 + e] = __uint_as_float(v1[e]);
-                    s[64 + e] = __uint_as_float(v2[e]);
-                    s[96 + e] = __uint_as_float(v3[e]);
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(&bars->s_empty[sb]);
-
-            // Scale, sheared bias, mask.  Fast path: the whole key tile is
-            // visible to this row and outside its bias band; then s keeps the
-            // raw q.k and the scale is folded into the exponent below.
-            const bool row_full = !valid || (j0 >= klo && j0 + C::BN <= khi);
-            const bool row_band = valid && band && j0 + C::BN - 1 >= pos - R + 1 && j0 <= pos;
-            const bool raw = row_full && !row_band && pos_scale;
-            float mk[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mk[i] = -CUDART_INF_F;
-            if (raw) {
-#pragma unroll
-                for (int k = 0; k < C::BN; ++k) mk[k & 7] = fmaxf(mk[k & 7], s[k]);
-            } else {
-                if (band && vec_bias) cp_async_wait(0);  // this row's window has landed
-                // Window offset of distance d = pos - j0 - k is o + 127 - k;
-                // outside [0, R) the window holds zeros.
-                const int o = (pos - j0 - (C::BN - 1)) - 8 * floor_div8(pos - j0 - (C::BN - 1));
-#pragma unroll
-                for (int k = 0; k < C::BN; ++k) {
-                    const int j = j0 + k;
-                    float bias = 0.f;
-                    if (row_band) {
-                        if constexpr (VEC) {
-                            bias = bf16_bits_to_f32(lds_u16(bias_row_s + 2 * (o + (C::BN - 1) - k)));
-                        } else {
-                            const int d = pos - j;
-                            if (d >= 0 && d < R) bias = bf16_bits_to_f32(__ldg(relg + rel_row + d));
-                        }
+                    for (int e = 0; e < 32; ++e) {
+                        s[e] = __uint_as_float(v0[e]);
+                        s[32 + e] = __uint_as_float(v1[e]);
                     }
-                    float v = fmaf(s[k], sl2, bias * kLog2e);
-                    if (!row_full && !(j >= klo && j < khi)) v = -CUDART_INF_F;
-                    s[k] = v;
-                    mk[k & 7] = fmaxf(mk[k & 7], v);
                 }
+                tc_fence_before();
+                mbar_arrive(&bars->s_empty[sb]);
+
+                // Scale, sheared bias, mask.  Fast path: the half tile is fully
+                // visible to this row and outside its bias band; then s keeps
+                // the raw q.k and the scale folds into the exponent below.
+                const bool row_full = !valid || (jh >= klo && jh + 64 <= khi);
+                const bool row_band = valid && band && jh + 63 >= pos - R + 1 && jh <= pos;
+                raw = row_full && !row_band && pos_scale;
+                float mk[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mk[i] = -CUDART_INF_F;
+                if (raw) {
+#pragma unroll
+                    for (int k = 0; k < 64; ++k) mk[k & 7] = fmaxf(mk[k & 7], s[k]);
+                } else {
+                    if (band && vec_bias) cp_async_wait(0);  // this half-row's window has landed
+                    const int dlo = pos - jh - 63;
+                    const uint16_t* win = bias_row + (dlo - 8 * floor_div8(dlo));  // + 63 - k
+#pragma unroll
+                    for (int k = 0; k < 64; ++k) {
+                        const int j = jh + k;
+                        float bias = 0.f;
+                        if (row_band) {
+                            if constexpr (VEC) {
+                                bias = bf16_bits_to_f32(win[63 - k]);
+                            } else {
+                                const int d = pos - j;
+                                if (d >= 0 && d < R) bias = bf16_bits_to_f32(__ldg(relg + rel_row + d));
+                            }
+                        }
+                        float v = fmaf(s[k], sl2, bias * kLog2e);
+                        if (!row_full && !(j >= klo && j < khi)) v = -CUDART_INF_F;
+                        s[k] = v;
+                        mk[k & 7] = fmaxf(mk[k & 7], v);
+                    }
+                }
+                mx = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])),
+                           fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
+                if (raw) mx *= sl2;
             }
+            // Exchange the half-row maxima (and the abort decision) with the partner half.
+            sXch[((sb * 2) + half) * 128 + r] = mx;
+            if (bar_or(1, C::kSoftThreads, my_abort)) {
+                any_abort = true;
+                break;
+            }
+            mx = fmaxf(mx, sXch[((sb * 2) + (half ^ 1)) * 128 + r]);
             if (band && vec_bias && jj + 1 < n_it && band_tile(key_block(jj + 1) * C::BN))
                 prefetch_bias(key_block(jj + 1) * C::BN);
-            float mx = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])),
-                             fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
-            if (raw) mx *= sl2;
             const float m_new = fmaxf(m_run, mx);
             const float mu = m_new == -CUDART_INF_F ? 0.f : m_new;
             const bool grow = m_run != -CUDART_INF_F && m_new > m_run;
             const float alpha = grow ? ex2(m_run - m_new) : 1.f;
 
-            // P_j into TMEM buffer jj % 2 once PV_{j-2} has read it.
+            // This half of P_j into TMEM buffer jj % 2 once PV_{j-2} has read it.
             if (!mbar_wait(&bars->p_free[sb], ((jj >> 1) & 1) ^ 1, p.timeout_ns, kSitePrefillPFull, p.err))
                 bars->abort = 1;
             float rs[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) rs[i] = 0.f;
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            {
                 uint32_t w[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const int k = c * 64 + 2 * e;
+                    const int k = 2 * e;
                     float a, bq;
                     if (raw) {
                         a = ex2(fmaf(s[k], sl2, -mu));
@@ -454,24 +471,26 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const AttnParams p) {
                     rs[(k + 1) & 7] += bq;
                     w[e] = pack_bf16(a, bq);
                 }
-                tmem_st32(lane_base + C::kPCol + 64 * sb + 32 * c, w);
+                tmem_st32(lane_base + C::kPCol + 64 * sb + 32 * half, w);
             }
             const float rsum = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
-            l_run = l_run * alpha + rsum;
+            l_half = l_half * alpha + rsum;
             m_run = m_new;
 
-            // Rescale the O row when its maximum grew (warp-collective TMEM access).
+            // Rescale this half of the O row when the row maximum grew
+            // (warp-collective TMEM access).
             if (jj >= 1 && __any_sync(0xffffffffu, grow)) {
                 if (!mbar_wait(&bars->o_done, (jj - 1) & 1, p.timeout_ns, kSitePrefillOFull, p.err)) bars->abort = 1;
                 tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < D / 64; ++c) {
                     uint32_t v[32];
-                    tmem_ld32(lane_base + C::kOCol + c * 32, v);
+                    const uint32_t ta = lane_base + C::kOCol + half * (D / 2) + c * 32;
+                    tmem_ld32(ta, v);
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                    tmem_st32(lane_base + C::kOCol + c * 32, v);
+                    tmem_st32(ta, v);
                 }
             }
             tmem_wait_st();
@@ -480,19 +499,24 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const AttnParams p) {
         }
         cp_async_wait(0);
 
-        // Epilogue: O / l.
-        const bool have = __all_sync(0xffffffffu, n_it > 0 && !aborted(bars));
+        // Epilogue: O / l, with l the sum of the two halves' partial sums.
+        // (buffer 2: the partner may still read buffer (n_it - 1) % 2 of the last tile)
+        sXch[(4 + half) * 128 + r] = l_half;
+        const bool failed = bar_or(1, C::kSoftThreads, any_abort || aborted(bars));
+        const float l_tot = sXch[4 * 128 + r] + sXch[5 * 128 + r];
+        const bool have = n_it > 0 && !failed;
         if (have) {
             if (!mbar_wait(&bars->o_final, 0, p.timeout_ns, kSitePrefillOFull, p.err)) bars->abort = 1;
             tc_fence_after();
         }
-        const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+        const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
         const bool partial = p.num_splits > 1;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
+            const int col = half * (D / 2) + c * 32;  // output dims [col, col + 32)
             uint32_t v[32];
             if (have) {
-                tmem_ld32(lane_base + C::kOCol + c * 32, v);
+                tmem_ld32(lane_base + C::kOCol + col, v);
                 tmem_wait_ld();
             } else {
 #pragma unroll
@@ -503,17 +527,17 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const AttnParams p) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(v[e]) * inv_l;
             if (partial) {
-                float* dst = p.ws_o + (((size_t)split * p.T + t) * p.H + h) * D + c * 32;
+                float* dst = p.ws_o + (((size_t)split * p.T + t) * p.H + h) * D + col;
 #pragma unroll
                 for (int e = 0; e < 32; e += 4)
                     *reinterpret_cast<float4*>(dst + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
             } else if (p.out_f32) {
-                float* dst = reinterpret_cast<float*>(p.out) + (size_t)t * p.o_st + (size_t)h * p.o_sh + c * 32;
+                float* dst = reinterpret_cast<float*>(p.out) + (size_t)t * p.o_st + (size_t)h * p.o_sh + col;
 #pragma unroll
                 for (int e = 0; e < 32; e += 4)
                     *reinterpret_cast<float4*>(dst + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
             } else {
-                uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + (size_t)t * p.o_st + (size_t)h * p.o_sh + c * 32;
+                uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + (size_t)t * p.o_st + (size_t)h * p.o_sh + col;
 #pragma unroll
                 for (int e = 0; e < 32; e += 8) {
                     uint4 pk;
@@ -525,8 +549,8 @@ __global__ void __launch_bounds__(256, 1) prefill_kernel(const AttnParams p) {
                 }
             }
         }
-        if (valid && partial)
-            p.ws_lse[((size_t)split * p.T + t) * p.H + h] = l_run > 0.f ? m_run + __log2f(l_run) : -CUDART_INF_F;
+        if (valid && partial && half == 0)
+            p.ws_lse[((size_t)split * p.T + t) * p.H + h] = l_tot > 0.f ? m_run + __log2f(l_tot) : -CUDART_INF_F;
     }
 
     tc_fence_before();
@@ -558,7 +582,7 @@ LaunchShape prefill_shape(const AttnParams& p) {
     const int tpt = 128 / p.G;
     const int qtiles = (p.max_seqlen_q + tpt - 1) / tpt;
     s.grid = dim3(qtiles, p.Hk, p.B * p.num_splits);
-    s.block = 256;
+    s.block = 384;
     s.smem = p.D == 128 ? prefill_smem_bytes<128>() : prefill_smem_bytes<64>();
     s.nstage = p.D == 128 ? PrefillCfg<128>::kStages : PrefillCfg<64>::kStages;
     return s;
