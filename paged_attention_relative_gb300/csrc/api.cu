@@ -96,7 +96,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // Paged cache (NB, BS, Hk, D) as a 4-D TMA tensor, innermost first:
 // (D, Hk, BS, NB), box (64 dims, 1 head, 16 slots, 1 block), 128-byte swizzle.
-[[maybe_unused]] rel_attn_status make_cache_map(const rel_attn_tensor* t, CUtensorMap* map, const char* name) {
+rel_attn_status make_cache_map(const rel_attn_tensor* t, CUtensorMap* map, const char* name) {
     auto enc = encode_fn();
     if (!enc) return fail(REL_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t dims[4] = {(cuuint64_t)t->shape[3], (cuuint64_t)t->shape[2], (cuuint64_t)t->shape[1],
@@ -399,6 +399,12 @@ extern "C" rel_attn_status rel_attn_paged_varlen(
     p.timeout_ns = wait_timeout_ns();
     p.err = dev->err;
 
+    CUtensorMap maps[2];
+    if (prefill) {
+        if ((st = make_cache_map(key_cache, &maps[0], "key_cache"))) return st;
+        if ((st = make_cache_map(value_cache, &maps[1], "value_cache"))) return st;
+    }
+
     // Splits: a cap, clamped to the 16-key slices a request can have.
     int64_t max_keys = MB * BS;
     int64_t splits = num_splits;
@@ -425,7 +431,7 @@ extern "C" rel_attn_status rel_attn_paged_varlen(
     p.nstage = shape.nstage;
     p.nprod = shape.nprod;
     if (t_ev_begin) cudaEventRecord(t_ev_begin, stream);
-    cudaError_t e = prefill ? launch_prefill(p, shape, stream) : launch_decode(p, shape, stream);
+    cudaError_t e = prefill ? launch_prefill(p, maps, shape, stream) : launch_decode(p, shape, stream);
     if (t_ev_end) cudaEventRecord(t_ev_end, stream);
     int launches = 1;
     if (e == cudaSuccess && splits > 1) {

@@ -53,9 +53,12 @@ struct LaunchShape {
 LaunchShape decode_shape(const AttnParams& p, int num_sms);
 cudaError_t launch_decode(const AttnParams& p, const LaunchShape& shape, cudaStream_t stream);
 
-// tcgen05 prefill kernel for 128-row GQA-packed query tiles.
+// tcgen05 prefill kernel for 128-row GQA-packed query tiles.  maps[0] / maps[1]
+// describe key_cache / value_cache as 4-D TMA tensors (D, Hk, BS, NB) with a
+// (64, 1, 16, 1) box and 128-byte swizzle.
 LaunchShape prefill_shape(const AttnParams& p);
-cudaError_t launch_prefill(const AttnParams& p, const LaunchShape& shape, cudaStream_t stream);
+cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap* maps, const LaunchShape& shape,
+                           cudaStream_t stream);
 
 // LSE-weighted merge of split partials into bf16 out.
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t stream);

@@ -8,12 +8,15 @@
 // and the bias band come first, so the running maximum settles early).
 //
 // Warp roles (384 threads):
-//   warps 0-2  Q/K/V producers: warp w gathers the 16-key pages w, w+3, w+6
-//              of Q (once) and of each K / V tile from the paged cache with
-//              16-byte cp.async (one block-table lookup per page, zero-fill
-//              outside the visible range) into 128-byte-swizzled tiles; after
-//              their copies land they fence the async proxy and arrive on the
-//              tile's full mbarrier.
+//   warp 0     Q/K/V producer: Q once with 16-byte cp.async (GQA-packed
+//              rows); each K / V tile as 2 KB TMA boxes (16 keys x 64 dims)
+//              straight from the paged cache, one per fully visible 16-key
+//              group, block-table entries fetched two tiles ahead; groups
+//              only partly inside the visible range go through
+//              zero-filling cp.async (proxy-fenced once landed).  Tiles are
+//              128-byte swizzled; the tile's full mbarrier takes the TMA
+//              bytes plus one arrival per producer lane.
+//   warps 1-2  idle.
 //   warp 3     MMA issuer (one thread) and TMEM owner: S_j = Q K_j^T into one
 //              of two TMEM buffers (M=128, N=128, K=head_dim), then
 //              O += P_{j-1} V_{j-1} with P read from TMEM and V from shared
@@ -57,13 +60,10 @@ struct PrefillCfg {
     static constexpr int kDB = D / 64;              // 64-dim (128-byte) column blocks
     static constexpr int kBlk = 128 * 128;          // one 128-row x 128-byte block
     static constexpr int kTileBytes = kDB * kBlk;   // a Q, K or V tile
-    static constexpr int kProdWarps = 3;
-    static constexpr int kProdThreads = 96;         // warps 0-2
     static constexpr int kMmaWarp = 3;
     static constexpr int kSoftThreads = 256;        // warps 4-11
     static constexpr int kThreads = 384;
     static constexpr int kStages = D == 128 ? 4 : 8;  // K/V ring slots (K even, V odd sequence numbers)
-    static constexpr int kLag = 2;                    // copy groups in flight per producer thread
     static constexpr int kBiasRow = 144;              // bytes of one half-row bias window (9 chunks)
     static constexpr int kBiasBytes = 2 * 128 * kBiasRow;
     static constexpr int kXchBytes = 3 * 2 * 128 * 4;  // half-row maxima (2 buffers), half-row sums
@@ -96,7 +96,9 @@ __device__ __forceinline__ int floor_div8(int x) { return x >= 0 ? x >> 3 : -((-
 // VEC: rel_logits rows are 16-byte aligned (R % 8 == 0), so bias windows are
 // staged by 16-byte copies; otherwise the bias is read per element.
 template <int D, bool VEC>
-__global__ void __launch_bounds__(384, 1) prefill_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(384, 1)
+    prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v) {
     using C = PrefillCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -147,9 +149,9 @@ __global__ void __launch_bounds__(384, 1) prefill_kernel(const AttnParams p) {
     auto band_tile = [&](int j0) { return R > 0 && pos_max - j0 >= 0 && pos_min - (j0 + C::BN - 1) < R; };
 
     if (threadIdx.x == 0) {
-        mbar_init(&bars->q_full, C::kProdThreads);
+        mbar_init(&bars->q_full, 32);
         for (int i = 0; i < C::kStages; ++i) {
-            mbar_init(&bars->kv_full[i], C::kProdThreads);
+            mbar_init(&bars->kv_full[i], 33);  // producer lanes + the expect_tx arrival
             mbar_init(&bars->kv_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -175,10 +177,14 @@ __global__ void __launch_bounds__(384, 1) prefill_kernel(const AttnParams p) {
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp < C::kProdWarps) {
-        // ------------------------------------------------------ Q/K/V producers
-        // Warp w copies the 16-row pages w, w+3, w+6 of every tile; one
-        // warp-wide copy covers kRows rows (kChunks lanes per 256- or 128-byte row).
+    if (warp == 0) {
+        // ------------------------------------------------------ Q/K/V producer
+        // Q: 16-byte cp.async per (row, chunk), GQA-packed rows, zero-fill
+        // past the tile's rows.  K/V: one TMA box (16 keys x 64 dims, 2 KB)
+        // per fully visible 16-key group and 64-dim block; groups that are
+        // only partly visible (or not at all) go through zero-filling
+        // cp.async, so V rows the softmax gives weight 0 hold zeros, never
+        // stale cache contents (0 * NaN would poison the row).
         constexpr int kChunks = D / 8;
         constexpr int kRows = 32 / kChunks;
         constexpr int kPerPage = 16 / kRows;
@@ -190,22 +196,17 @@ __global__ void __launch_bounds__(384, 1) prefill_kernel(const AttnParams p) {
         const uint64_t pol_first = l2_policy_evict_first();
         const uint64_t pol_last = l2_policy_evict_last();
         const uint32_t col_off = (lchunk >> 3) * C::kBlk;
-        // lane_off walks this lane's rows inside a page; within a page row
-        // (16*pg + kk*kRows + lrow) & 7 == ((kk*kRows) & 7) | lrow, so the
-        // swizzle is the per-lane constant cx XOR a compile-time one.
+        // Within a 16-row group, row (kk*kRows + lrow) & 7 == ((kk*kRows) & 7) | lrow,
+        // so the 128-byte swizzle is the per-lane constant cx XOR a compile-time one.
         const long long lane_off = (long long)lrow * p.c_s1 + lchunk * 8;
         const long long row_step = (long long)kRows * p.c_s1;
         const uint32_t cx = (uint32_t)((lchunk & 7) ^ lrow);
-        const uint32_t dst_lane = col_off + lrow * 128 + 0u;
-        int issued = 0, done = 0;
-        auto complete = [&](int k) {  // copy group k of this thread has landed
-            fence_proxy_async_smem();
-            if (k == 0)
-                mbar_arrive(&bars->q_full);
-            else
-                mbar_arrive(&bars->kv_full[(k - 1) % C::kStages]);
-        };
-        for (int pg = warp; pg < 8; pg += C::kProdWarps) {  // Q tile (group 0)
+        const uint32_t dst_lane = col_off + lrow * 128;
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+        }
+        for (int pg = 0; pg < 8; ++pg) {
 #pragma unroll
             for (int kk = 0; kk < kPerPage; ++kk) {
                 const int r = 16 * pg + kk * kRows + lrow;
@@ -218,54 +219,93 @@ __global__ void __launch_bounds__(384, 1) prefill_kernel(const AttnParams p) {
             }
         }
         cp_async_commit();
-        ++issued;
+        // At most one cp.async group is in flight: the Q tile, then the
+        // partial groups of a stage.  It is retired (landed, proxy-fenced,
+        // one arrival per lane) after the next stage has been issued, or
+        // before the producer blocks on a full ring.
+        uint64_t* pend = &bars->q_full;
+        auto retire = [&](int newer) {
+            cp_async_wait(newer);
+            fence_proxy_async_smem();
+            mbar_arrive(pend);
+            pend = nullptr;
+        };
+        // Block-table entries run two tiles ahead of the copies: lane l < 8
+        // holds the physical block of 16-key group l of a tile.
+        auto load_bt = [&](int jj) -> int {
+            int v = 0;
+            if (lane < 8 && jj < n_it) {
+                const int jg = key_block(jj) * C::BN + 16 * lane;
+                if (jg + 15 >= lo && jg < hi) v = __ldg(bt + jg / p.BS);
+            }
+            return v;
+        };
+        int bt_cur = load_bt(0), bt_n1 = load_bt(1), bt_n2 = load_bt(2);
+        // TMA lanes: lane -> (16-key group lane / kDB, 64-dim block lane % kDB).
+        const int t_pg = lane / C::kDB, t_db = lane % C::kDB;
         for (int seq = 0; seq < 2 * n_it; ++seq) {
             const int slot = seq % C::kStages;
             const int round = seq / C::kStages;
             // Never block on a full ring while holding copies whose landing has
             // not been signalled: the consumer may be waiting for exactly those.
             if (!mbar_try_wait(&bars->kv_empty[slot], (round & 1) ^ 1)) {
-                while (done < issued) {
-                    cp_async_wait(issued - done - 1);
-                    complete(done++);
-                }
+                if (pend) retire(0);
                 if (!mbar_wait(&bars->kv_empty[slot], (round & 1) ^ 1, p.timeout_ns, kSitePrefillKEmpty, p.err))
                     bars->abort = 1;
             }
             if (__any_sync(0xffffffffu, aborted(bars))) break;
+            if (seq >= 2 && (seq & 1) == 0) {
+                bt_cur = bt_n1;
+                bt_n1 = bt_n2;
+                bt_n2 = load_bt((seq >> 1) + 2);
+            }
             const int j0 = key_block(seq >> 1) * C::BN;
-            const uint16_t* cache = (seq & 1) ? vc : kc;
-            const uint32_t dst_tile = smem_u32(sKV + slot * C::kTileBytes) + dst_lane;
-            for (int pg = warp; pg < 8; pg += C::kProdWarps) {
-                const int jg = j0 + 16 * pg;
-                long long poff = 0;
-                if (lane == 0 && jg + 15 >= lo && jg < hi) {
-                    const int blk = min(max(__ldg(bt + jg / p.BS), 0), p.NB - 1);
-                    poff = (long long)blk * p.c_s0 + (long long)(jg % p.BS) * p.c_s1 + (long long)g * p.c_s2;
-                }
-                poff = __shfl_sync(0xffffffffu, poff, 0);
-                const bool page_full = jg >= lo && jg + 16 <= hi;
-                const uint16_t* src = cache + poff + lane_off;
+            // Bit pg set: 16-key group pg is fully visible (whole-box TMA).
+            uint32_t full_mask = 0;
 #pragma unroll
-                for (int kk = 0; kk < kPerPage; ++kk) {
-                    const int row = kk * kRows + lrow;  // key jg + row
-                    const bool valid = page_full || (jg + row >= lo && jg + row < hi);
-                    const uint32_t dst = dst_tile + (16 * pg + kk * kRows) * 128 + ((cx ^ ((kk * kRows) & 7)) << 4);
-                    cp_async_16(dst, valid ? src : cache, valid ? 16u : 0u, pol_last);
-                    src += row_step;
+            for (int pg = 0; pg < 8; ++pg) {
+                const int jg = j0 + 16 * pg;
+                if (jg >= lo && jg + 16 <= hi) full_mask |= 1u << pg;
+            }
+            uint64_t* full_bar = &bars->kv_full[slot];
+            uint8_t* tile = sKV + slot * C::kTileBytes;
+            if (lane == 0) mbar_arrive_expect_tx(full_bar, (uint32_t)__popc(full_mask) * C::kDB * 2048u);
+            __syncwarp();
+            const int blk_t = min(max(__shfl_sync(0xffffffffu, bt_cur, t_pg & 7), 0), p.NB - 1);
+            if (lane < 8 * C::kDB && ((full_mask >> t_pg) & 1)) {
+                const int jg = j0 + 16 * t_pg;
+                tma_load_4d_hint(tile + t_db * C::kBlk + t_pg * 16 * 128, (seq & 1) ? &tm_v : &tm_k, full_bar,
+                                 64 * t_db, g, jg % p.BS, blk_t, pol_last);
+            }
+            const bool part = full_mask != 0xffu;
+            if (part) {
+                const uint16_t* cache = (seq & 1) ? vc : kc;
+                const uint32_t dst_tile = smem_u32(tile) + dst_lane;
+                for (int pg = 0; pg < 8; ++pg) {
+                    if ((full_mask >> pg) & 1) continue;
+                    const int jg = j0 + 16 * pg;
+                    const int blk = min(max(__shfl_sync(0xffffffffu, bt_cur, pg), 0), p.NB - 1);
+                    const uint16_t* src = cache + (long long)blk * p.c_s0 + (long long)(jg % p.BS) * p.c_s1 +
+                                          (long long)g * p.c_s2 + lane_off;
+#pragma unroll
+                    for (int kk = 0; kk < kPerPage; ++kk) {
+                        const int row = kk * kRows + lrow;  // key jg + row
+                        const bool valid = jg + row >= lo && jg + row < hi;
+                        const uint32_t dst =
+                            dst_tile + (16 * pg + kk * kRows) * 128 + ((cx ^ ((kk * kRows) & 7)) << 4);
+                        cp_async_16(dst, valid ? src : cache, valid ? 16u : 0u, pol_last);
+                        src += row_step;
+                    }
                 }
+                cp_async_commit();
             }
-            cp_async_commit();
-            ++issued;
-            if (issued - done > C::kLag) {
-                cp_async_wait(C::kLag);
-                complete(done++);
-            }
+            if (pend) retire(part ? 1 : 0);
+            if (part)
+                pend = full_bar;
+            else
+                mbar_arrive(full_bar);
         }
-        while (done < issued) {
-            cp_async_wait(issued - done - 1);
-            complete(done++);
-        }
+        if (pend) retire(0);
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0 && n_it > 0) {
@@ -567,11 +607,11 @@ int prefill_smem_bytes() {
 }
 
 template <int D, bool VEC>
-cudaError_t launch_t(const AttnParams& p, const LaunchShape& s, cudaStream_t stream) {
+cudaError_t launch_t(const AttnParams& p, const CUtensorMap* maps, const LaunchShape& s, cudaStream_t stream) {
     auto kern = prefill_kernel<D, VEC>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, s.smem);
     if (e != cudaSuccess) return e;
-    kern<<<s.grid, s.block, s.smem, stream>>>(p);
+    kern<<<s.grid, s.block, s.smem, stream>>>(p, maps[0], maps[1]);
     return cudaGetLastError();
 }
 
@@ -588,10 +628,11 @@ LaunchShape prefill_shape(const AttnParams& p) {
     return s;
 }
 
-cudaError_t launch_prefill(const AttnParams& p, const LaunchShape& s, cudaStream_t stream) {
+cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap* maps, const LaunchShape& s,
+                           cudaStream_t stream) {
     const bool vec = p.vec_bias != 0;
-    if (p.D == 128) return vec ? launch_t<128, true>(p, s, stream) : launch_t<128, false>(p, s, stream);
-    if (p.D == 64) return vec ? launch_t<64, true>(p, s, stream) : launch_t<64, false>(p, s, stream);
+    if (p.D == 128) return vec ? launch_t<128, true>(p, maps, s, stream) : launch_t<128, false>(p, maps, s, stream);
+    if (p.D == 64) return vec ? launch_t<64, true>(p, maps, s, stream) : launch_t<64, false>(p, maps, s, stream);
     return cudaErrorInvalidValue;
 }
 
