@@ -53,6 +53,8 @@ namespace relattn {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
+// CTAs per cluster: adjacent query tiles that share (multicast) every K/V tile.
+constexpr int kCluster = 2;
 
 template <int D>
 struct PrefillCfg {
@@ -118,19 +120,37 @@ __global__ void __launch_bounds__(384, 1)
     const int sq = p.cu_seqlens_q[b + 1] - q0;
     const int sk = p.cache_seqlens[b];
     const int i0 = qt * TPT;
-    if (i0 >= sq) return;  // CTA-uniform, before any barrier
     const int i1 = min(sq, i0 + TPT);
-    const int n_rows = (i1 - i0) * G;
+    const int n_rows = max(i1 - i0, 0) * G;
     const int off = sk - sq;
     const int pos_min = i0 + off, pos_max = i1 - 1 + off;
     const int R = p.R;
 
-    // Keys any row of the tile may see, as 128-key tiles, split contiguously.
-    int hi = sk;
-    if (p.causal) hi = min(hi, pos_max + 1);
-    if (p.wr >= 0) hi = min(hi, pos_max + p.wr + 1);
-    int lo = 0;
-    if (p.wl >= 0) lo = max(0, pos_min - p.wl);
+    // The kCluster CTAs of a cluster hold adjacent query tiles of one (request,
+    // kv head, split) and walk one shared sequence of K/V tiles: the union of
+    // their visible ranges.  Rank r holds tile qt_top - r; CTAs whose tile is
+    // past the request's end are inactive (no loads, no MMAs).
+    const int crank = (int)cluster_ctarank();
+    const int qt_top = qt + crank;
+    uint32_t active = 0;
+#pragma unroll
+    for (int r = 0; r < kCluster; ++r)
+        if ((qt_top - r) * TPT < sq) active |= 1u << r;
+    const bool me_active = (active >> crank) & 1;
+    const int n_act = __popc(active);
+    const int my_idx = __popc(active & ((1u << crank) - 1));
+    const uint16_t mc_mask = (uint16_t)active;
+    const int u_i0 = (qt_top - (kCluster - 1)) * TPT;                       // lowest tile of the cluster
+    const int u_i1 = min(sq, (qt_top - (active ? __ffs(active) - 1 : 0) + 1) * TPT);  // end of the highest active one
+
+    // Keys any row of the cluster's tiles may see, as 128-key tiles, split contiguously.
+    int hi = sk, lo = 0;
+    if (active) {
+        const int u_pmin = u_i0 + off, u_pmax = u_i1 - 1 + off;
+        if (p.causal) hi = min(hi, u_pmax + 1);
+        if (p.wr >= 0) hi = min(hi, u_pmax + p.wr + 1);
+        if (p.wl >= 0) lo = max(0, u_pmin - p.wl);
+    }
     int kb_first = 0, n_tiles = 0;
     if (hi > lo) {
         kb_first = lo / C::BN;
@@ -152,7 +172,7 @@ __global__ void __launch_bounds__(384, 1)
         mbar_init(&bars->q_full, 32);
         for (int i = 0; i < C::kStages; ++i) {
             mbar_init(&bars->kv_full[i], 33);  // producer lanes + the expect_tx arrival
-            mbar_init(&bars->kv_empty[i], 1);
+            mbar_init(&bars->kv_empty[i], n_act);  // one MMA commit per active CTA of the cluster
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->s_full[i], 1);
@@ -164,6 +184,13 @@ __global__ void __launch_bounds__(384, 1)
         mbar_init(&bars->o_final, 1);
         bars->abort = 0;
         fence_mbar_init();
+    }
+    // Peers multicast into this CTA's ring and arrive on its barriers only
+    // after every CTA of the cluster has initialised them.
+    cluster_sync();
+    if (!me_active) {
+        cluster_sync();
+        return;
     }
     if (warp == C::kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -272,10 +299,10 @@ __global__ void __launch_bounds__(384, 1)
             if (lane == 0) mbar_arrive_expect_tx(full_bar, (uint32_t)__popc(full_mask) * C::kDB * 2048u);
             __syncwarp();
             const int blk_t = min(max(__shfl_sync(0xffffffffu, bt_cur, t_pg & 7), 0), p.NB - 1);
-            if (lane < 8 * C::kDB && ((full_mask >> t_pg) & 1)) {
+            if (lane < 8 * C::kDB && ((full_mask >> t_pg) & 1) && lane % n_act == my_idx) {
                 const int jg = j0 + 16 * t_pg;
-                tma_load_4d_hint(tile + t_db * C::kBlk + t_pg * 16 * 128, (seq & 1) ? &tm_v : &tm_k, full_bar,
-                                 64 * t_db, g, jg % p.BS, blk_t, pol_last);
+                tma_load_4d_mc(tile + t_db * C::kBlk + t_pg * 16 * 128, (seq & 1) ? &tm_v : &tm_k, full_bar,
+                               64 * t_db, g, jg % p.BS, blk_t, mc_mask, pol_last);
             }
             const bool part = full_mask != 0xffu;
             if (part) {
@@ -306,6 +333,16 @@ __global__ void __launch_bounds__(384, 1)
                 mbar_arrive(full_bar);
         }
         if (pend) retire(0);
+        // Wait until every active CTA has released each slot for the last
+        // time: afterwards no peer commit is still travelling to this CTA.
+        if (!__any_sync(0xffffffffu, aborted(bars))) {
+            for (int sl = 0; sl < min(C::kStages, 2 * n_it); ++sl) {
+                const int last = sl + C::kStages * ((2 * n_it - 1 - sl) / C::kStages);
+                if (!mbar_wait(&bars->kv_empty[sl], (last / C::kStages) & 1, p.timeout_ns, kSitePrefillKEmpty,
+                               p.err))
+                    bars->abort = 1;
+            }
+        }
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0 && n_it > 0) {
@@ -330,7 +367,7 @@ __global__ void __launch_bounds__(384, 1)
                     umma_bf16_tmem_a(tmem + C::kOCol, pcol + kk * 8, db, idPV, (t > 0 || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(&bars->o_done);
-                umma_commit(&bars->kv_empty[slot]);
+                umma_commit_mc(&bars->kv_empty[slot], mc_mask);
                 umma_commit(&bars->p_free[pb]);
             };
             for (int jj = 0; jj < n_it && ok; ++jj) {
@@ -351,7 +388,7 @@ __global__ void __launch_bounds__(384, 1)
                     umma_bf16(tmem + sb * C::BN, da, db, idS, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(&bars->s_full[sb]);
-                umma_commit(&bars->kv_empty[slot]);
+                umma_commit_mc(&bars->kv_empty[slot], mc_mask);
                 if (jj >= 1) issue_pv(jj - 1);
             }
             if (ok) issue_pv(n_it - 1);
@@ -599,6 +636,7 @@ __global__ void __launch_bounds__(384, 1)
     if (warp == C::kMmaWarp)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(C::kTmemCols)
                      : "memory");
+    cluster_sync();
 }
 
 template <int D>
@@ -611,7 +649,20 @@ cudaError_t launch_t(const AttnParams& p, const CUtensorMap* maps, const LaunchS
     auto kern = prefill_kernel<D, VEC>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, s.smem);
     if (e != cudaSuccess) return e;
-    kern<<<s.grid, s.block, s.smem, stream>>>(p, maps[0], maps[1]);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = s.grid;
+    cfg.blockDim = dim3((unsigned)s.block);
+    cfg.dynamicSmemBytes = (size_t)s.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p, maps[0], maps[1]);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -621,7 +672,7 @@ LaunchShape prefill_shape(const AttnParams& p) {
     LaunchShape s;
     const int tpt = 128 / p.G;
     const int qtiles = (p.max_seqlen_q + tpt - 1) / tpt;
-    s.grid = dim3(qtiles, p.Hk, p.B * p.num_splits);
+    s.grid = dim3((qtiles + kCluster - 1) / kCluster * kCluster, p.Hk, p.B * p.num_splits);
     s.block = 384;
     s.smem = p.D == 128 ? prefill_smem_bytes<128>() : prefill_smem_bytes<64>();
     s.nstage = p.D == 128 ? PrefillCfg<128>::kStages : PrefillCfg<64>::kStages;
