@@ -94,6 +94,22 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+// rel_logits (T, H, R) as a 3-D TMA tensor, innermost first: (R, H, T), box
+// (144 distances, G heads, ts tokens), no swizzle; needs R % 8 == 0.
+rel_attn_status make_rel_map(const rel_attn_tensor* t, int G, int ts, CUtensorMap* map) {
+    auto enc = encode_fn();
+    if (!enc) return fail(REL_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[3] = {(cuuint64_t)t->shape[2], (cuuint64_t)t->shape[1], (cuuint64_t)t->shape[0]};
+    cuuint64_t strides[2] = {(cuuint64_t)t->stride[1] * 2, (cuuint64_t)t->stride[0] * 2};
+    cuuint32_t box[3] = {144, (cuuint32_t)G, (cuuint32_t)ts};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, t->data, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(REL_ATTN_ERR_UNSUPPORTED, "rel_logits: TMA descriptor rejected (CUresult %d)", (int)r);
+    return REL_ATTN_OK;
+}
+
 // Paged cache (NB, BS, Hk, D) as a 4-D TMA tensor, innermost first:
 // (D, Hk, BS, NB), box (64 dims, 1 head, 16 slots, 1 block), 128-byte swizzle.
 rel_attn_status make_cache_map(const rel_attn_tensor* t, CUtensorMap* map, const char* name) {
@@ -392,6 +408,7 @@ extern "C" rel_attn_status rel_attn_paged_varlen(
     p.D = (int32_t)D;
     p.max_rows = (int32_t)(rows > INT32_MAX ? INT32_MAX : rows);
     p.max_seqlen_q = max_seqlen_q;
+    p.scale = softmax_scale;
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
     p.causal = causal ? 1 : 0;
     p.wl = window_left;
@@ -399,10 +416,19 @@ extern "C" rel_attn_status rel_attn_paged_varlen(
     p.timeout_ns = wait_timeout_ns();
     p.err = dev->err;
 
-    CUtensorMap maps[2];
+    CUtensorMap maps[3];
+    std::memset(maps, 0, sizeof maps);
     if (prefill) {
         if ((st = make_cache_map(key_cache, &maps[0], "key_cache"))) return st;
         if ((st = make_cache_map(value_cache, &maps[1], "value_cache"))) return st;
+        // Tokens per rel_logits box: the largest divisor of the tile's 128 / G
+        // tokens that is at most 8 (a box then never crosses the tile).
+        const int tpt = (int)(128 / G);
+        int ts = 1;
+        for (int d = 1; d <= 8 && d <= tpt; ++d)
+            if (tpt % d == 0) ts = d;
+        p.bias_ts = ts;
+        if (p.vec_bias && (st = make_rel_map(rel_logits, (int)G, ts, &maps[2]))) return st;
     }
 
     // Splits: a cap, clamped to the 16-key slices a request can have.

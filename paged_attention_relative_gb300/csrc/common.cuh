@@ -147,6 +147,15 @@ __device__ __forceinline__ void tma_load_4d_mc(void* dst, const void* desc, uint
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d_hint(void* dst, const void* desc, uint64_t* bar, int c0, int c1, int c2,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(desc)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+        : "memory");
+}
+
 // ---------------------------------------------------------------- clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

@@ -31,7 +31,9 @@ struct AttnParams {
     int32_t num_splits;
     int32_t max_rows;          // max_seqlen_q * G (decode: <= 64)
     int32_t max_seqlen_q;
+    float scale;               // softmax_scale
     float scale_log2;          // softmax_scale * log2(e)
+    int32_t bias_ts;           // prefill: tokens per rel_logits TMA box (divides 128 / G, <= 8)
     int32_t causal, wl, wr;
     int32_t nstage;
     int32_t nprod;             // decode: producer warps
@@ -55,7 +57,8 @@ cudaError_t launch_decode(const AttnParams& p, const LaunchShape& shape, cudaStr
 
 // tcgen05 prefill kernel for 128-row GQA-packed query tiles.  maps[0] / maps[1]
 // describe key_cache / value_cache as 4-D TMA tensors (D, Hk, BS, NB) with a
-// (64, 1, 16, 1) box and 128-byte swizzle.
+// (64, 1, 16, 1) box and 128-byte swizzle; maps[2] describes rel_logits as a
+// 3-D tensor (R, H, T) with a (144, G, bias_ts) box (only read when vec_bias).
 LaunchShape prefill_shape(const AttnParams& p);
 cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap* maps, const LaunchShape& shape,
                            cudaStream_t stream);

@@ -24,15 +24,20 @@
 //   warps 4-11 softmax: warps 4-7 take keys [0, 64) of every tile and warps
 //              8-11 keys [64, 128); warp w reads TMEM lanes 32*(w%4).. so
 //              thread (w, lane) owns half of row 32*(w%4) + lane.  Per tile it
-//              reads its half of S_j, applies scale, the sheared relative bias
-//              and the mask, exchanges the half-row maximum with its partner
-//              through shared memory (one named barrier per tile), keeps the
-//              fp32 online softmax (base 2), writes its half of P_j into TMEM
-//              as bf16 pairs, rescales its half of the O row when the row
-//              maximum grew, and writes its half of the output.  For key tiles
-//              that reach the row's bias band it prefetches, one band tile
-//              ahead, its 144-byte window of rel_logits (16-byte aligned, the
-//              64 distances its half needs) into shared memory with cp.async.
+//              reads its half of S_j, forms sc * q.k + bias (natural units;
+//              tiles outside every row's bias band keep the raw q.k and fold
+//              the scale into the exponent), masks only when some row of the
+//              warp does not see the whole half tile, exchanges the half-row
+//              maximum with its partner through shared memory (one named
+//              barrier per tile), keeps the fp32 online softmax, writes its
+//              half of P_j into TMEM as bf16 pairs, rescales its half of the O
+//              row when the row maximum grew, and writes its half of the
+//              output.  The bias of a band tile is staged by TMA (thread 128
+//              issues it once the previous band tile's windows are consumed):
+//              one 144-value window per (token, head) row, starting at the
+//              16-byte aligned distance below the row's token sub-box, zero
+//              outside [0, R), so the sheared gather becomes a reversed
+//              shared-memory read.
 // Every mbarrier wait is bounded; on timeout the kernel records the site in
 // the device error word and winds down.
 //
@@ -66,8 +71,9 @@ struct PrefillCfg {
     static constexpr int kSoftThreads = 256;        // warps 4-11
     static constexpr int kThreads = 384;
     static constexpr int kStages = D == 128 ? 4 : 8;  // K/V ring slots (K even, V odd sequence numbers)
-    static constexpr int kBiasRow = 144;              // bytes of one half-row bias window (9 chunks)
-    static constexpr int kBiasBytes = 2 * 128 * kBiasRow;
+    static constexpr int kBiasW = 144;                // rel_logits values per staged bias row
+    // 128 rows, plus up to 16 token sub-boxes each padded to a 128-byte boundary
+    static constexpr int kBiasBytes = 128 * kBiasW * 2 + 16 * 128;
     static constexpr int kXchBytes = 3 * 2 * 128 * 4;  // half-row maxima (2 buffers), half-row sums
     static constexpr int kData = kTileBytes + kStages * kTileBytes + kBiasBytes + kXchBytes;
     static constexpr int kTmemCols = 512;
@@ -85,6 +91,7 @@ struct PrefillBars {
     uint64_t p_free[2];
     uint64_t o_done;   // one phase per PV tile (rescale waits, never more than one phase behind)
     uint64_t o_final;  // single phase: every MMA of the CTA has completed
+    uint64_t bias_full;  // one phase per band tile: its rel_logits windows have landed
     uint32_t tmem_base;
     int abort;
 };
@@ -100,7 +107,7 @@ __device__ __forceinline__ int floor_div8(int x) { return x >= 0 ? x >> 3 : -((-
 template <int D, bool VEC>
 __global__ void __launch_bounds__(384, 1)
     prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v) {
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_rel) {
     using C = PrefillCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -182,6 +189,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         mbar_init(&bars->o_done, 1);
         mbar_init(&bars->o_final, 1);
+        mbar_init(&bars->bias_full, 1);
         bars->abort = 0;
         fence_mbar_init();
     }
@@ -403,7 +411,8 @@ __global__ void __launch_bounds__(384, 1)
         const int half = (warp - 4) >> 2;  // keys [64*half, 64*half + 64) of each tile
         const int r = (warp & 3) * 32 + lane;  // row == TMEM lane
         const bool valid = r < n_rows;
-        const int tok = i0 + (valid ? r / G : 0);
+        const int i_rel = valid ? r / G : 0;  // token within the tile
+        const int tok = i0 + i_rel;
         const int hh = valid ? r % G : 0;
         const int t = q0 + tok, h = g * G + hh;
         const int pos = tok + off;
@@ -415,37 +424,45 @@ __global__ void __launch_bounds__(384, 1)
         if (p.wl >= 0) klo = max(0, pos - p.wl);
         const uint16_t* relg = reinterpret_cast<const uint16_t*>(p.rel);
         const size_t rel_row = ((size_t)t * p.H + h) * (size_t)R;
-        uint8_t* my_bias = sBias + (half * 128 + r) * C::kBiasRow;
-        const uint16_t* bias_row = reinterpret_cast<const uint16_t*>(my_bias);
-        const uint32_t bias_dst = smem_u32(my_bias);
-        const uint64_t pol_first = l2_policy_evict_first();
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-        const float sl2 = p.scale_log2;
-        const bool pos_scale = sl2 > 0.f;
+        const float sc = p.scale;          // scores are kept in natural units: sc * q.k + bias
+        const float sl2 = p.scale_log2;    // sc * log2(e)
+        const bool pos_scale = sc > 0.f;
         const int kh = 64 * half;  // first key of this half within a tile
         float m_run = -CUDART_INF_F, l_half = 0.f;
         bool any_abort = false;
 
-        // Band tiles form one contiguous run of jj; prefetch this half-row's
-        // window for the first one, then for each next one while the current
-        // one is in use.  Distance of key k (in the half) is d_lo + 63 - k.
-        auto prefetch_bias = [&](int j0n) {
-            const int qa = floor_div8(pos - j0n - kh - 63);
-#pragma unroll
-            for (int i = 0; i < C::kBiasRow / 16; ++i) {
-                const int q = qa + i;
-                const bool ok = valid && q >= 0 && 8 * q + 8 <= R;
-                cp_async_16(bias_dst + 16 * i, ok ? relg + rel_row + 8 * q : relg, ok ? 16u : 0u, pol_first);
+        // Bias windows (VEC): a band tile's rel_logits arrive by TMA as rows of
+        // kBiasW values, one row per (token, head) of the tile, each starting at
+        // the 16-byte aligned distance below the smallest distance its token
+        // sub-box needs (zero-filled outside [0, R)).  Key k of the tile reads
+        // element e_r + 127 - k of row r.
+        const int TS = p.bias_ts, n_sub = TPT / TS;
+        const int sub_bytes = (TS * G * C::kBiasW * 2 + 127) & ~127;  // TMA destinations are 128-byte aligned
+        const int i_sub = (i_rel / TS) * TS;
+        const int e_r = (i_rel - i_sub) + ((i0 + i_sub + off - 127) & 7);
+        const uint16_t* win = reinterpret_cast<const uint16_t*>(sBias + (i_rel / TS) * sub_bytes +
+                                                                (r - i_sub * G) * (C::kBiasW * 2)) +
+                              e_r + 127 - kh;
+        auto issue_bias = [&](int j0n) {  // one thread; the previous window is no longer read
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&bars->bias_full, (uint32_t)(n_sub * TS * G * C::kBiasW * 2));
+            const uint64_t pol = l2_policy_evict_first();
+            for (int sbx = 0; sbx < n_sub; ++sbx) {
+                const int ts = i0 + sbx * TS;
+                const int a = ts + off - j0n - 127;
+                tma_load_3d_hint(sBias + sbx * sub_bytes, &tm_rel, &bars->bias_full, a - (a & 7),
+                                 g * G, q0 + ts, pol);
             }
-            cp_async_commit();
         };
-        if (vec_bias) {
+        if (VEC && threadIdx.x == 128) {
             for (int jj = 0; jj < n_it; ++jj)
                 if (band_tile(key_block(jj) * C::BN)) {
-                    prefetch_bias(key_block(jj) * C::BN);
+                    issue_bias(key_block(jj) * C::BN);
                     break;
                 }
         }
+        int nb = 0;  // band tiles consumed
 
         for (int jj = 0; jj < n_it; ++jj) {
             const int sb = jj & 1;
@@ -456,7 +473,9 @@ __global__ void __launch_bounds__(384, 1)
             my_abort = __any_sync(0xffffffffu, my_abort || aborted(bars));
             float s[64];
             float mx = -CUDART_INF_F;
-            bool raw = false;
+            // raw: s keeps q.k (no bias on this tile); the scale folds into
+            // the exponent.  Otherwise s holds sc * q.k + bias.
+            const bool raw = !band && pos_scale;
             if (!my_abort) {
                 tc_fence_after();
                 {
@@ -473,43 +492,44 @@ __global__ void __launch_bounds__(384, 1)
                 tc_fence_before();
                 mbar_arrive(&bars->s_empty[sb]);
 
-                // Scale, sheared bias, mask.  Fast path: the half tile is fully
-                // visible to this row and outside its bias band; then s keeps
-                // the raw q.k and the scale folds into the exponent below.
+                if (!raw) {
+                    if (band) {
+                        if constexpr (VEC) {
+                            if (!mbar_wait(&bars->bias_full, nb & 1, p.timeout_ns, kSitePrefillRelFull, p.err))
+                                bars->abort = 1;
+#pragma unroll
+                            for (int k = 0; k < 64; ++k) s[k] = fmaf(s[k], sc, bf16_bits_to_f32(win[-k]));
+                        } else {
+#pragma unroll 8
+                            for (int k = 0; k < 64; ++k) {
+                                const int d = pos - (jh + k);
+                                const float bias =
+                                    valid && d >= 0 && d < R ? bf16_bits_to_f32(__ldg(relg + rel_row + d)) : 0.f;
+                                s[k] = fmaf(s[k], sc, bias);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 64; ++k) s[k] *= sc;
+                    }
+                }
+                // Mask (warp-uniform skip when every row of the warp sees the whole half tile).
                 const bool row_full = !valid || (jh >= klo && jh + 64 <= khi);
-                const bool row_band = valid && band && jh + 63 >= pos - R + 1 && jh <= pos;
-                raw = row_full && !row_band && pos_scale;
-                float mk[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mk[i] = -CUDART_INF_F;
-                if (raw) {
-#pragma unroll
-                    for (int k = 0; k < 64; ++k) mk[k & 7] = fmaxf(mk[k & 7], s[k]);
-                } else {
-                    if (band && vec_bias) cp_async_wait(0);  // this half-row's window has landed
-                    const int dlo = pos - jh - 63;
-                    const uint16_t* win = bias_row + (dlo - 8 * floor_div8(dlo));  // + 63 - k
+                if (!__all_sync(0xffffffffu, row_full)) {
 #pragma unroll
                     for (int k = 0; k < 64; ++k) {
                         const int j = jh + k;
-                        float bias = 0.f;
-                        if (row_band) {
-                            if constexpr (VEC) {
-                                bias = bf16_bits_to_f32(win[63 - k]);
-                            } else {
-                                const int d = pos - j;
-                                if (d >= 0 && d < R) bias = bf16_bits_to_f32(__ldg(relg + rel_row + d));
-                            }
-                        }
-                        float v = fmaf(s[k], sl2, bias * kLog2e);
-                        if (!row_full && !(j >= klo && j < khi)) v = -CUDART_INF_F;
-                        s[k] = v;
-                        mk[k & 7] = fmaxf(mk[k & 7], v);
+                        if (!row_full && !(j >= klo && j < khi)) s[k] = -CUDART_INF_F;
                     }
                 }
+                float mk[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mk[i] = -CUDART_INF_F;
+#pragma unroll
+                for (int k = 0; k < 64; ++k) mk[k & 7] = fmaxf(mk[k & 7], s[k]);
                 mx = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])),
                            fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
-                if (raw) mx *= sl2;
+                if (raw) mx *= sc;
             }
             // Exchange the half-row maxima (and the abort decision) with the partner half.
             sXch[((sb * 2) + half) * 128 + r] = mx;
@@ -518,12 +538,16 @@ __global__ void __launch_bounds__(384, 1)
                 break;
             }
             mx = fmaxf(mx, sXch[((sb * 2) + (half ^ 1)) * 128 + r]);
-            if (band && vec_bias && jj + 1 < n_it && band_tile(key_block(jj + 1) * C::BN))
-                prefetch_bias(key_block(jj + 1) * C::BN);
+            if (band) {
+                ++nb;
+                if (VEC && threadIdx.x == 128 && jj + 1 < n_it && band_tile(key_block(jj + 1) * C::BN))
+                    issue_bias(key_block(jj + 1) * C::BN);
+            }
             const float m_new = fmaxf(m_run, mx);
-            const float mu = m_new == -CUDART_INF_F ? 0.f : m_new;
+            const float ml = m_new == -CUDART_INF_F ? 0.f : m_new * kLog2e;
             const bool grow = m_run != -CUDART_INF_F && m_new > m_run;
-            const float alpha = grow ? ex2(m_run - m_new) : 1.f;
+            const float alpha = grow ? ex2((m_run - m_new) * kLog2e) : 1.f;
+            const float c1 = raw ? sl2 : kLog2e;
 
             // This half of P_j into TMEM buffer jj % 2 once PV_{j-2} has read it.
             if (!mbar_wait(&bars->p_free[sb], ((jj >> 1) & 1) ^ 1, p.timeout_ns, kSitePrefillPFull, p.err))
@@ -536,14 +560,8 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const int k = 2 * e;
-                    float a, bq;
-                    if (raw) {
-                        a = ex2(fmaf(s[k], sl2, -mu));
-                        bq = ex2(fmaf(s[k + 1], sl2, -mu));
-                    } else {
-                        a = ex2(s[k] - mu);
-                        bq = ex2(s[k + 1] - mu);
-                    }
+                    const float a = ex2(fmaf(s[k], c1, -ml));
+                    const float bq = ex2(fmaf(s[k + 1], c1, -ml));
                     rs[k & 7] += a;
                     rs[(k + 1) & 7] += bq;
                     w[e] = pack_bf16(a, bq);
@@ -574,7 +592,6 @@ __global__ void __launch_bounds__(384, 1)
             tc_fence_before();
             mbar_arrive(&bars->p_full[sb]);
         }
-        cp_async_wait(0);
 
         // Epilogue: O / l, with l the sum of the two halves' partial sums.
         // (buffer 2: the partner may still read buffer (n_it - 1) % 2 of the last tile)
@@ -627,7 +644,8 @@ __global__ void __launch_bounds__(384, 1)
             }
         }
         if (valid && partial && half == 0)
-            p.ws_lse[((size_t)split * p.T + t) * p.H + h] = l_tot > 0.f ? m_run + __log2f(l_tot) : -CUDART_INF_F;
+            p.ws_lse[((size_t)split * p.T + t) * p.H + h] =
+                l_tot > 0.f ? m_run * kLog2e + __log2f(l_tot) : -CUDART_INF_F;
     }
 
     tc_fence_before();
@@ -661,7 +679,7 @@ cudaError_t launch_t(const AttnParams& p, const CUtensorMap* maps, const LaunchS
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, p, maps[0], maps[1]);
+    e = cudaLaunchKernelEx(&cfg, kern, p, maps[0], maps[1], maps[2]);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
