@@ -16,7 +16,10 @@
 //              zero-filling cp.async (proxy-fenced once landed).  Tiles are
 //              128-byte swizzled; the tile's full mbarrier takes the TMA
 //              bytes plus one arrival per producer lane.
-//   warps 1-2  idle.
+//   warp 1     bias windows: for each band tile (one that reaches some row's
+//              bias band) it stages that tile's rel_logits by TMA once the
+//              softmax warps have read the previous band tile's (see below).
+//   warp 2     idle.
 //   warp 3     MMA issuer (one thread) and TMEM owner: S_j = Q K_j^T into one
 //              of two TMEM buffers (M=128, N=128, K=head_dim), then
 //              O += P_{j-1} V_{j-1} with P read from TMEM and V from shared
@@ -32,8 +35,9 @@
 //              barrier per tile), keeps the fp32 online softmax, writes its
 //              half of P_j into TMEM as bf16 pairs, rescales its half of the O
 //              row when the row maximum grew, and writes its half of the
-//              output.  The bias of a band tile is staged by TMA (thread 128
-//              issues it once the previous band tile's windows are consumed):
+//              output.  The reference maximum moves lazily (only when the
+//              row maximum exceeds it by more than 2^8), so O is rarely
+//              rescaled.  The bias of a band tile is staged by warp 1:
 //              one 144-value window per (token, head) row, starting at the
 //              16-byte aligned distance below the row's token sub-box, zero
 //              outside [0, R), so the sheared gather becomes a reversed
@@ -58,6 +62,8 @@ namespace relattn {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
+// Lazy rescaling threshold: 8 in log2 units, in natural units.
+constexpr float kLazyRescale = 8.0f * 0.6931471805599453f;
 // CTAs per cluster: adjacent query tiles that share (multicast) every K/V tile.
 constexpr int kCluster = 2;
 
@@ -91,7 +97,8 @@ struct PrefillBars {
     uint64_t p_free[2];
     uint64_t o_done;   // one phase per PV tile (rescale waits, never more than one phase behind)
     uint64_t o_final;  // single phase: every MMA of the CTA has completed
-    uint64_t bias_full;  // one phase per band tile: its rel_logits windows have landed
+    uint64_t bias_full;   // one phase per band tile: its rel_logits windows have landed
+    uint64_t bias_empty;  // one phase per band tile: every softmax warp has read its windows
     uint32_t tmem_base;
     int abort;
 };
@@ -190,6 +197,7 @@ __global__ void __launch_bounds__(384, 1)
         mbar_init(&bars->o_done, 1);
         mbar_init(&bars->o_final, 1);
         mbar_init(&bars->bias_full, 1);
+        mbar_init(&bars->bias_empty, C::kSoftThreads / 32);
         bars->abort = 0;
         fence_mbar_init();
     }
@@ -351,6 +359,38 @@ __global__ void __launch_bounds__(384, 1)
                     bars->abort = 1;
             }
         }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ bias windows
+        // Band tile n's rel_logits, once every softmax warp has finished
+        // reading band tile n-1's: one TMA box per token sub-box of TS tokens
+        // (all G heads), rows of kBiasW distances from the 16-byte aligned
+        // distance below the sub-box's smallest one.
+        if (VEC && lane == 0) {
+            const int TS = p.bias_ts, n_sub = TPT / TS;
+            const int sub_bytes = (TS * G * C::kBiasW * 2 + 127) & ~127;
+            const uint64_t pol = l2_policy_evict_first();
+            int nbi = 0;
+            for (int jj = 0; jj < n_it; ++jj) {
+                const int j0 = key_block(jj) * C::BN;
+                if (!band_tile(j0)) continue;
+                if (nbi > 0 && !mbar_wait(&bars->bias_empty, (nbi - 1) & 1, p.timeout_ns, kSitePrefillRelEmpty,
+                                          p.err)) {
+                    bars->abort = 1;
+                    break;
+                }
+                if (aborted(bars)) break;
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(&bars->bias_full, (uint32_t)(n_sub * TS * G * C::kBiasW * 2));
+                for (int sbx = 0; sbx < n_sub; ++sbx) {
+                    const int ts = i0 + sbx * TS;
+                    const int a = ts + off - j0 - 127;
+                    tma_load_3d_hint(sBias + sbx * sub_bytes, &tm_rel, &bars->bias_full, a - (a & 7), g * G,
+                                     q0 + ts, pol);
+                }
+                ++nbi;
+            }
+        }
+        __syncwarp();
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0 && n_it > 0) {
@@ -437,31 +477,13 @@ __global__ void __launch_bounds__(384, 1)
         // the 16-byte aligned distance below the smallest distance its token
         // sub-box needs (zero-filled outside [0, R)).  Key k of the tile reads
         // element e_r + 127 - k of row r.
-        const int TS = p.bias_ts, n_sub = TPT / TS;
+        const int TS = p.bias_ts;
         const int sub_bytes = (TS * G * C::kBiasW * 2 + 127) & ~127;  // TMA destinations are 128-byte aligned
         const int i_sub = (i_rel / TS) * TS;
         const int e_r = (i_rel - i_sub) + ((i0 + i_sub + off - 127) & 7);
         const uint16_t* win = reinterpret_cast<const uint16_t*>(sBias + (i_rel / TS) * sub_bytes +
                                                                 (r - i_sub * G) * (C::kBiasW * 2)) +
                               e_r + 127 - kh;
-        auto issue_bias = [&](int j0n) {  // one thread; the previous window is no longer read
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(&bars->bias_full, (uint32_t)(n_sub * TS * G * C::kBiasW * 2));
-            const uint64_t pol = l2_policy_evict_first();
-            for (int sbx = 0; sbx < n_sub; ++sbx) {
-                const int ts = i0 + sbx * TS;
-                const int a = ts + off - j0n - 127;
-                tma_load_3d_hint(sBias + sbx * sub_bytes, &tm_rel, &bars->bias_full, a - (a & 7),
-                                 g * G, q0 + ts, pol);
-            }
-        };
-        if (VEC && threadIdx.x == 128) {
-            for (int jj = 0; jj < n_it; ++jj)
-                if (band_tile(key_block(jj) * C::BN)) {
-                    issue_bias(key_block(jj) * C::BN);
-                    break;
-                }
-        }
         int nb = 0;  // band tiles consumed
 
         for (int jj = 0; jj < n_it; ++jj) {
@@ -471,7 +493,7 @@ __global__ void __launch_bounds__(384, 1)
             const bool band = band_tile(j0);
             bool my_abort = !mbar_wait(&bars->s_full[sb], (jj >> 1) & 1, p.timeout_ns, kSitePrefillSFull, p.err);
             my_abort = __any_sync(0xffffffffu, my_abort || aborted(bars));
-            float s[64];
+            float2 s[32];  // keys (kh + 2e, kh + 2e + 1) of the tile
             float mx = -CUDART_INF_F;
             // raw: s keeps q.k (no bias on this tile); the scale folds into
             // the exponent.  Otherwise s holds sc * q.k + bias.
@@ -484,51 +506,65 @@ __global__ void __launch_bounds__(384, 1)
                     tmem_ld32(lane_base + sb * C::BN + kh + 32, v1);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        s[e] = __uint_as_float(v0[e]);
-                        s[32 + e] = __uint_as_float(v1[e]);
+                    for (int e = 0; e < 16; ++e) {
+                        s[e] = make_float2(__uint_as_float(v0[2 * e]), __uint_as_float(v0[2 * e + 1]));
+                        s[16 + e] = make_float2(__uint_as_float(v1[2 * e]), __uint_as_float(v1[2 * e + 1]));
                     }
                 }
                 tc_fence_before();
                 mbar_arrive(&bars->s_empty[sb]);
 
                 if (!raw) {
+                    const float2 sc2 = make_float2(sc, sc);
                     if (band) {
                         if constexpr (VEC) {
                             if (!mbar_wait(&bars->bias_full, nb & 1, p.timeout_ns, kSitePrefillRelFull, p.err))
                                 bars->abort = 1;
 #pragma unroll
-                            for (int k = 0; k < 64; ++k) s[k] = fmaf(s[k], sc, bf16_bits_to_f32(win[-k]));
+                            for (int e = 0; e < 32; ++e)
+                                s[e] = __ffma2_rn(s[e], sc2,
+                                                  make_float2(bf16_bits_to_f32(win[-2 * e]),
+                                                              bf16_bits_to_f32(win[-2 * e - 1])));
+                            // Every read of this band tile's windows is done.
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&bars->bias_empty);
                         } else {
-#pragma unroll 8
-                            for (int k = 0; k < 64; ++k) {
-                                const int d = pos - (jh + k);
-                                const float bias =
+#pragma unroll 4
+                            for (int e = 0; e < 32; ++e) {
+                                const int d = pos - (jh + 2 * e);
+                                const float b0 =
                                     valid && d >= 0 && d < R ? bf16_bits_to_f32(__ldg(relg + rel_row + d)) : 0.f;
-                                s[k] = fmaf(s[k], sc, bias);
+                                const float b1 = valid && d - 1 >= 0 && d - 1 < R
+                                                     ? bf16_bits_to_f32(__ldg(relg + rel_row + d - 1))
+                                                     : 0.f;
+                                s[e] = __ffma2_rn(s[e], sc2, make_float2(b0, b1));
                             }
                         }
                     } else {
 #pragma unroll
-                        for (int k = 0; k < 64; ++k) s[k] *= sc;
+                        for (int e = 0; e < 32; ++e) s[e] = __fmul2_rn(s[e], sc2);
                     }
                 }
                 // Mask (warp-uniform skip when every row of the warp sees the whole half tile).
                 const bool row_full = !valid || (jh >= klo && jh + 64 <= khi);
                 if (!__all_sync(0xffffffffu, row_full)) {
 #pragma unroll
-                    for (int k = 0; k < 64; ++k) {
-                        const int j = jh + k;
-                        if (!row_full && !(j >= klo && j < khi)) s[k] = -CUDART_INF_F;
+                    for (int e = 0; e < 32; ++e) {
+                        const int j = jh + 2 * e;
+                        if (!row_full && !(j >= klo && j < khi)) s[e].x = -CUDART_INF_F;
+                        if (!row_full && !(j + 1 >= klo && j + 1 < khi)) s[e].y = -CUDART_INF_F;
                     }
                 }
                 float mk[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) mk[i] = -CUDART_INF_F;
+                for (int i = 0; i < 8; ++i) mk[i] = fmax3(s[i].x, s[i].y, s[8 + i].x);
 #pragma unroll
-                for (int k = 0; k < 64; ++k) mk[k & 7] = fmaxf(mk[k & 7], s[k]);
-                mx = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])),
-                           fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
+                for (int i = 0; i < 8; ++i) mk[i] = fmax3(mk[i], s[8 + i].y, s[16 + i].x);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mk[i] = fmax3(mk[i], s[16 + i].y, s[24 + i].x);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mk[i] = fmaxf(mk[i], s[24 + i].y);
+                mx = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]), fmaxf(mk[6], mk[7]));
                 if (raw) mx *= sc;
             }
             // Exchange the half-row maxima (and the abort decision) with the partner half.
@@ -538,41 +574,40 @@ __global__ void __launch_bounds__(384, 1)
                 break;
             }
             mx = fmaxf(mx, sXch[((sb * 2) + (half ^ 1)) * 128 + r]);
-            if (band) {
-                ++nb;
-                if (VEC && threadIdx.x == 128 && jj + 1 < n_it && band_tile(key_block(jj + 1) * C::BN))
-                    issue_bias(key_block(jj + 1) * C::BN);
-            }
-            const float m_new = fmaxf(m_run, mx);
-            const float ml = m_new == -CUDART_INF_F ? 0.f : m_new * kLog2e;
-            const bool grow = m_run != -CUDART_INF_F && m_new > m_run;
-            const float alpha = grow ? ex2((m_run - m_new) * kLog2e) : 1.f;
+            if (band) ++nb;
+            // Lazy rescaling: the reference maximum m_run only moves when the
+            // row maximum exceeds it by more than 8 in log2 units, so P stays
+            // below 2^8 and O is rescaled rarely; O / l is unchanged.
+            const float m_tile = fmaxf(m_run, mx);
+            const bool grow = m_run != -CUDART_INF_F && m_tile > m_run + kLazyRescale;
+            const float m_use = (m_run == -CUDART_INF_F || grow) ? m_tile : m_run;
+            const float ml = m_use == -CUDART_INF_F ? 0.f : m_use * kLog2e;
+            const float alpha = grow ? ex2((m_run - m_use) * kLog2e) : 1.f;
             const float c1 = raw ? sl2 : kLog2e;
 
             // This half of P_j into TMEM buffer jj % 2 once PV_{j-2} has read it.
             if (!mbar_wait(&bars->p_free[sb], ((jj >> 1) & 1) ^ 1, p.timeout_ns, kSitePrefillPFull, p.err))
                 bars->abort = 1;
-            float rs[8];
+            float2 rs[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) rs[i] = 0.f;
+            for (int i = 0; i < 4; ++i) rs[i] = make_float2(0.f, 0.f);
             {
+                const float2 c12 = make_float2(c1, c1), nml = make_float2(-ml, -ml);
                 uint32_t w[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const int k = 2 * e;
-                    const float a = ex2(fmaf(s[k], c1, -ml));
-                    const float bq = ex2(fmaf(s[k + 1], c1, -ml));
-                    rs[k & 7] += a;
-                    rs[(k + 1) & 7] += bq;
-                    w[e] = pack_bf16(a, bq);
+                    const float2 x = __ffma2_rn(s[e], c12, nml);
+                    const float2 pe = make_float2(ex2(x.x), ex2(x.y));
+                    rs[e & 3] = __fadd2_rn(rs[e & 3], pe);
+                    w[e] = pack_bf16(pe.x, pe.y);
                 }
                 tmem_st32(lane_base + C::kPCol + 64 * sb + 32 * half, w);
             }
-            const float rsum = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
-            l_half = l_half * alpha + rsum;
-            m_run = m_new;
+            const float2 rs2 = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
+            l_half = l_half * alpha + (rs2.x + rs2.y);
+            m_run = m_use;
 
-            // Rescale this half of the O row when the row maximum grew
+            // Rescale this half of the O row when the reference maximum moved
             // (warp-collective TMEM access).
             if (jj >= 1 && __any_sync(0xffffffffu, grow)) {
                 if (!mbar_wait(&bars->o_done, (jj - 1) & 1, p.timeout_ns, kSitePrefillOFull, p.err)) bars->abort = 1;

@@ -10,7 +10,7 @@ import torch
 
 from oracle import reference as ref
 from paged_attention_relative_gb300.workloads import chunked_prefill, make_case, mixed_window
-from tests.gpu_util import TOL_SPLIT, assert_close, assert_no_device_error, run, to_dev
+from tests.gpu_util import assert_close, assert_no_device_error, run, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -67,7 +67,14 @@ def test_prefill_split_matches_single_fp32():
     b = torch.empty_like(a)
     run(c, g, num_splits=4, out=a)
     run(c, g, num_splits=1, out=b)
-    assert (a - b).abs().max().item() <= TOL_SPLIT
+    # Both paths round every softmax weight p to bf16 (relative error <= 2^-9)
+    # against their own reference maximum and keep everything else in fp32, so
+    # each lies within 2^-9 * sum_j (p_j / l) |v_j| of the exact output and
+    # the two within twice that: the attention of |V|, from the oracle.
+    bound = torch.from_numpy(ref.forward(c.with_(value_cache=c.value_cache.abs()))).float().cuda()
+    diff = (a - b).abs()
+    assert (diff <= 2.0 ** -8 * bound + 1e-5).all(), f"split vs single {diff.max().item():.3e}"
+    assert diff.mean().item() <= 1e-4
     assert_close(a, ref.forward(c), tol_max=5e-3, tol_mean=5e-4, what="fp32 out")
 
 
