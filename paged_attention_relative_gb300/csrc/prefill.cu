@@ -8,18 +8,21 @@
 // and the bias band come first, so the running maximum settles early).
 //
 // Warp roles (384 threads):
-//   warp 0     Q/K/V producer: Q once with 16-byte cp.async (GQA-packed
-//              rows); each K / V tile as 2 KB TMA boxes (16 keys x 64 dims)
-//              straight from the paged cache, one per fully visible 16-key
-//              group, block-table entries fetched two tiles ahead; groups
-//              only partly inside the visible range go through
-//              zero-filling cp.async (proxy-fenced once landed).  Tiles are
-//              128-byte swizzled; the tile's full mbarrier takes the TMA
-//              bytes plus one arrival per producer lane.
+//   warps 0, 2 producers: warp 0 loads Q once with 16-byte cp.async
+//              (GQA-packed rows), then the K tiles; warp 2 the V tiles, each
+//              into its own ring so K never waits behind a V slot.  A tile
+//              arrives as 2 KB TMA boxes (16 keys x 64 dims) straight from the
+//              paged cache, one per fully visible 16-key group, multicast to
+//              the other CTA of the cluster (the two take turns issuing), with
+//              block-table entries fetched two tiles ahead; groups only
+//              partly inside the visible range go through zero-filling
+//              cp.async (proxy-fenced once landed).  Tiles are 128-byte
+//              swizzled; a slot's full mbarrier takes the TMA bytes plus one
+//              arrival per producer lane, its empty mbarrier one MMA commit
+//              per CTA of the cluster.
 //   warp 1     bias windows: for each band tile (one that reaches some row's
 //              bias band) it stages that tile's rel_logits by TMA once the
 //              softmax warps have read the previous band tile's (see below).
-//   warp 2     idle.
 //   warp 3     MMA issuer (one thread) and TMEM owner: S_j = Q K_j^T into one
 //              of two TMEM buffers (M=128, N=128, K=head_dim), then
 //              O += P_{j-1} V_{j-1} with P read from TMEM and V from shared
@@ -76,7 +79,8 @@ struct PrefillCfg {
     static constexpr int kMmaWarp = 3;
     static constexpr int kSoftThreads = 256;        // warps 4-11
     static constexpr int kThreads = 384;
-    static constexpr int kStages = D == 128 ? 4 : 8;  // K/V ring slots (K even, V odd sequence numbers)
+    static constexpr int kStages = D == 128 ? 4 : 8;  // K/V tile slots: a K ring, then a V ring
+    static constexpr int kRing = kStages / 2;
     static constexpr int kBiasW = 144;                // rel_logits values per staged bias row
     // 128 rows, plus up to 16 token sub-boxes each padded to a 128-byte boundary
     static constexpr int kBiasBytes = 128 * kBiasW * 2 + 16 * 128;
@@ -220,21 +224,25 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp == 0) {
-        // ------------------------------------------------------ Q/K/V producer
+    if (warp == 0 || warp == 2) {
+        // ------------------------------------------------------ Q/K and V producers
+        // Warp 0 loads Q, then the K ring; warp 2 the V ring, so a K tile
+        // never queues behind a V slot the softmax still holds.
         // Q: 16-byte cp.async per (row, chunk), GQA-packed rows, zero-fill
         // past the tile's rows.  K/V: one TMA box (16 keys x 64 dims, 2 KB)
-        // per fully visible 16-key group and 64-dim block; groups that are
+        // per fully visible 16-key group and 64-dim block, multicast to the
+        // cluster (the active CTAs take turns issuing them); groups that are
         // only partly visible (or not at all) go through zero-filling
         // cp.async, so V rows the softmax gives weight 0 hold zeros, never
         // stale cache contents (0 * NaN would poison the row).
+        const bool is_v = warp == 2;
         constexpr int kChunks = D / 8;
         constexpr int kRows = 32 / kChunks;
         constexpr int kPerPage = 16 / kRows;
         const int lrow = lane / kChunks, lchunk = lane % kChunks;
         const uint16_t* qg = reinterpret_cast<const uint16_t*>(p.q);
-        const uint16_t* kc = reinterpret_cast<const uint16_t*>(p.k_cache);
-        const uint16_t* vc = reinterpret_cast<const uint16_t*>(p.v_cache);
+        const uint16_t* cache = reinterpret_cast<const uint16_t*>(is_v ? p.v_cache : p.k_cache);
+        const CUtensorMap* tmap = is_v ? &tm_v : &tm_k;
         const int32_t* bt = p.block_table + (size_t)b * p.bt_stride;
         const uint64_t pol_first = l2_policy_evict_first();
         const uint64_t pol_last = l2_policy_evict_last();
@@ -245,28 +253,29 @@ __global__ void __launch_bounds__(384, 1)
         const long long row_step = (long long)kRows * p.c_s1;
         const uint32_t cx = (uint32_t)((lchunk & 7) ^ lrow);
         const uint32_t dst_lane = col_off + lrow * 128;
-        if (lane == 0) {
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
-        }
-        for (int pg = 0; pg < 8; ++pg) {
-#pragma unroll
-            for (int kk = 0; kk < kPerPage; ++kk) {
-                const int r = 16 * pg + kk * kRows + lrow;
-                const bool valid = r < n_rows;
-                const int tok = i0 + r / G, hh = r % G;
-                const uint16_t* src = qg + (size_t)(q0 + tok) * p.q_st + (size_t)(g * G + hh) * p.q_sh + lchunk * 8;
-                const uint32_t dst =
-                    smem_u32(sQ) + dst_lane + (16 * pg + kk * kRows) * 128 + ((cx ^ ((kk * kRows) & 7)) << 4);
-                cp_async_16(dst, valid ? src : qg, valid ? 16u : 0u, pol_first);
-            }
-        }
-        cp_async_commit();
+        if (lane == 0) tma_prefetch_desc(tmap);
         // At most one cp.async group is in flight: the Q tile, then the
         // partial groups of a stage.  It is retired (landed, proxy-fenced,
         // one arrival per lane) after the next stage has been issued, or
         // before the producer blocks on a full ring.
-        uint64_t* pend = &bars->q_full;
+        uint64_t* pend = nullptr;
+        if (!is_v) {
+            for (int pg = 0; pg < 8; ++pg) {
+#pragma unroll
+                for (int kk = 0; kk < kPerPage; ++kk) {
+                    const int r = 16 * pg + kk * kRows + lrow;
+                    const bool valid = r < n_rows;
+                    const int tok = i0 + r / G, hh = r % G;
+                    const uint16_t* src =
+                        qg + (size_t)(q0 + tok) * p.q_st + (size_t)(g * G + hh) * p.q_sh + lchunk * 8;
+                    const uint32_t dst =
+                        smem_u32(sQ) + dst_lane + (16 * pg + kk * kRows) * 128 + ((cx ^ ((kk * kRows) & 7)) << 4);
+                    cp_async_16(dst, valid ? src : qg, valid ? 16u : 0u, pol_first);
+                }
+            }
+            cp_async_commit();
+            pend = &bars->q_full;
+        }
         auto retire = [&](int newer) {
             cp_async_wait(newer);
             fence_proxy_async_smem();
@@ -286,9 +295,10 @@ __global__ void __launch_bounds__(384, 1)
         int bt_cur = load_bt(0), bt_n1 = load_bt(1), bt_n2 = load_bt(2);
         // TMA lanes: lane -> (16-key group lane / kDB, 64-dim block lane % kDB).
         const int t_pg = lane / C::kDB, t_db = lane % C::kDB;
-        for (int seq = 0; seq < 2 * n_it; ++seq) {
-            const int slot = seq % C::kStages;
-            const int round = seq / C::kStages;
+        const int ring0 = is_v ? C::kRing : 0;
+        for (int jj = 0; jj < n_it; ++jj) {
+            const int slot = ring0 + jj % C::kRing;
+            const int round = jj / C::kRing;
             // Never block on a full ring while holding copies whose landing has
             // not been signalled: the consumer may be waiting for exactly those.
             if (!mbar_try_wait(&bars->kv_empty[slot], (round & 1) ^ 1)) {
@@ -297,12 +307,12 @@ __global__ void __launch_bounds__(384, 1)
                     bars->abort = 1;
             }
             if (__any_sync(0xffffffffu, aborted(bars))) break;
-            if (seq >= 2 && (seq & 1) == 0) {
+            if (jj >= 1) {
                 bt_cur = bt_n1;
                 bt_n1 = bt_n2;
-                bt_n2 = load_bt((seq >> 1) + 2);
+                bt_n2 = load_bt(jj + 2);
             }
-            const int j0 = key_block(seq >> 1) * C::BN;
+            const int j0 = key_block(jj) * C::BN;
             // Bit pg set: 16-key group pg is fully visible (whole-box TMA).
             uint32_t full_mask = 0;
 #pragma unroll
@@ -317,12 +327,11 @@ __global__ void __launch_bounds__(384, 1)
             const int blk_t = min(max(__shfl_sync(0xffffffffu, bt_cur, t_pg & 7), 0), p.NB - 1);
             if (lane < 8 * C::kDB && ((full_mask >> t_pg) & 1) && lane % n_act == my_idx) {
                 const int jg = j0 + 16 * t_pg;
-                tma_load_4d_mc(tile + t_db * C::kBlk + t_pg * 16 * 128, (seq & 1) ? &tm_v : &tm_k, full_bar,
-                               64 * t_db, g, jg % p.BS, blk_t, mc_mask, pol_last);
+                tma_load_4d_mc(tile + t_db * C::kBlk + t_pg * 16 * 128, tmap, full_bar, 64 * t_db, g, jg % p.BS,
+                               blk_t, mc_mask, pol_last);
             }
             const bool part = full_mask != 0xffu;
             if (part) {
-                const uint16_t* cache = (seq & 1) ? vc : kc;
                 const uint32_t dst_tile = smem_u32(tile) + dst_lane;
                 for (int pg = 0; pg < 8; ++pg) {
                     if ((full_mask >> pg) & 1) continue;
@@ -352,10 +361,10 @@ __global__ void __launch_bounds__(384, 1)
         // Wait until every active CTA has released each slot for the last
         // time: afterwards no peer commit is still travelling to this CTA.
         if (!__any_sync(0xffffffffu, aborted(bars))) {
-            for (int sl = 0; sl < min(C::kStages, 2 * n_it); ++sl) {
-                const int last = sl + C::kStages * ((2 * n_it - 1 - sl) / C::kStages);
-                if (!mbar_wait(&bars->kv_empty[sl], (last / C::kStages) & 1, p.timeout_ns, kSitePrefillKEmpty,
-                               p.err))
+            for (int i = 0; i < min(C::kRing, n_it); ++i) {
+                const int last = i + C::kRing * ((n_it - 1 - i) / C::kRing);
+                if (!mbar_wait(&bars->kv_empty[ring0 + i], (last / C::kRing) & 1, p.timeout_ns,
+                               kSitePrefillKEmpty, p.err))
                     bars->abort = 1;
             }
         }
@@ -400,10 +409,9 @@ __global__ void __launch_bounds__(384, 1)
             bool ok = mbar_wait(&bars->q_full, 0, p.timeout_ns, kSitePrefillLoadQ, p.err);
             auto issue_pv = [&](int t) {
                 const int pb = t & 1;
-                const int seq = 2 * t + 1;
-                const int slot = seq % C::kStages;
+                const int slot = C::kRing + t % C::kRing;
                 ok = ok && mbar_wait(&bars->p_full[pb], (t >> 1) & 1, p.timeout_ns, kSitePrefillPFull, p.err);
-                ok = ok && mbar_wait(&bars->kv_full[slot], (seq / C::kStages) & 1, p.timeout_ns, kSitePrefillVFull,
+                ok = ok && mbar_wait(&bars->kv_full[slot], (t / C::kRing) & 1, p.timeout_ns, kSitePrefillVFull,
                                      p.err);
                 if (!ok) return;
                 tc_fence_after();
@@ -420,9 +428,8 @@ __global__ void __launch_bounds__(384, 1)
             };
             for (int jj = 0; jj < n_it && ok; ++jj) {
                 const int sb = jj & 1;
-                const int seq = 2 * jj;
-                const int slot = seq % C::kStages;
-                ok = ok && mbar_wait(&bars->kv_full[slot], (seq / C::kStages) & 1, p.timeout_ns, kSitePrefillKFull,
+                const int slot = jj % C::kRing;
+                ok = ok && mbar_wait(&bars->kv_full[slot], (jj / C::kRing) & 1, p.timeout_ns, kSitePrefillKFull,
                                      p.err);
                 ok = ok && mbar_wait(&bars->s_empty[sb], ((jj >> 1) & 1) ^ 1, p.timeout_ns, kSitePrefillSEmpty,
                                      p.err);
