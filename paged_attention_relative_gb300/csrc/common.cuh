@@ -271,6 +271,22 @@ __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tme
         : "memory");
 }
 
+// Same two with a compile-time accumulate flag (no predicate set-up between
+// back-to-back MMAs).
+template <int ACC>
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, %4;" ::"r"(d_tmem), "l"(a_desc),
+                 "l"(b_desc), "r"(idesc), "n"(ACC)
+                 : "memory");
+}
+
+template <int ACC>
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc) {
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, %4;" ::"r"(d_tmem), "r"(a_tmem),
+                 "l"(b_desc), "r"(idesc), "n"(ACC)
+                 : "memory");
+}
+
 // Arrive once on the mbarrier when every tcgen05 operation this thread issued
 // so far has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {

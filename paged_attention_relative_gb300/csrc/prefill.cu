@@ -407,21 +407,35 @@ __global__ void __launch_bounds__(384, 1)
             constexpr uint32_t idPV = umma_idesc_bf16(128, D, true);
             const uint32_t aQ = smem_u32(sQ), aKV = smem_u32(sKV);
             bool ok = mbar_wait(&bars->q_full, 0, p.timeout_ns, kSitePrefillLoadQ, p.err);
+            // Descriptors are formed before each wait, so the MMAs of a tile
+            // issue back to back (any instruction between two of them delays
+            // the tensor pipe).  A descriptor's low bits hold address / 16, so
+            // a byte offset inside shared memory adds offset / 16.
+            uint64_t dQ[D / 16];
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) dQ[kk] = umma_desc_sw128(aQ + (kk >> 2) * C::kBlk + (kk & 3) * 32, 16, 1024);
+            const uint64_t dK0 = umma_desc_sw128(aKV, 16, 1024);
+            const uint64_t dV0 = umma_desc_sw128(aKV, C::kBlk, 1024);
             auto issue_pv = [&](int t) {
                 const int pb = t & 1;
                 const int slot = C::kRing + t % C::kRing;
+                const uint64_t dv = dV0 + (uint64_t)((slot * C::kTileBytes) >> 4);
+                uint64_t dV[C::BN / 16];
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 16; ++kk) dV[kk] = dv + (uint64_t)((kk * 16 * 128) >> 4);
+                const uint32_t pcol = tmem + C::kPCol + 64 * pb;
+                const uint32_t od = tmem + C::kOCol;
                 ok = ok && mbar_wait(&bars->p_full[pb], (t >> 1) & 1, p.timeout_ns, kSitePrefillPFull, p.err);
                 ok = ok && mbar_wait(&bars->kv_full[slot], (t / C::kRing) & 1, p.timeout_ns, kSitePrefillVFull,
                                      p.err);
                 if (!ok) return;
                 tc_fence_after();
-                const uint32_t vbase = aKV + slot * C::kTileBytes;
-                const uint32_t pcol = tmem + C::kPCol + 64 * pb;
+                if (t > 0)
+                    umma_ts<1>(od, pcol, dV[0], idPV);
+                else
+                    umma_ts<0>(od, pcol, dV[0], idPV);
 #pragma unroll
-                for (int kk = 0; kk < C::BN / 16; ++kk) {
-                    const uint64_t db = umma_desc_sw128(vbase + kk * 16 * 128, C::kBlk, 1024);
-                    umma_bf16_tmem_a(tmem + C::kOCol, pcol + kk * 8, db, idPV, (t > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 1; kk < C::BN / 16; ++kk) umma_ts<1>(od, pcol + kk * 8, dV[kk], idPV);
                 umma_commit(&bars->o_done);
                 umma_commit_mc(&bars->kv_empty[slot], mc_mask);
                 umma_commit(&bars->p_free[pb]);
@@ -429,19 +443,20 @@ __global__ void __launch_bounds__(384, 1)
             for (int jj = 0; jj < n_it && ok; ++jj) {
                 const int sb = jj & 1;
                 const int slot = jj % C::kRing;
+                const uint64_t dk = dK0 + (uint64_t)((slot * C::kTileBytes) >> 4);
+                uint64_t dK[D / 16];
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) dK[kk] = dk + (uint64_t)((((kk >> 2) * C::kBlk) + (kk & 3) * 32) >> 4);
+                const uint32_t sd = tmem + sb * C::BN;
                 ok = ok && mbar_wait(&bars->kv_full[slot], (jj / C::kRing) & 1, p.timeout_ns, kSitePrefillKFull,
                                      p.err);
                 ok = ok && mbar_wait(&bars->s_empty[sb], ((jj >> 1) & 1) ^ 1, p.timeout_ns, kSitePrefillSEmpty,
                                      p.err);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t kbase = aKV + slot * C::kTileBytes;
+                umma_ss<0>(sd, dQ[0], dK[0], idS);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t da = umma_desc_sw128(aQ + (kk >> 2) * C::kBlk + (kk & 3) * 32, 16, 1024);
-                    const uint64_t db = umma_desc_sw128(kbase + (kk >> 2) * C::kBlk + (kk & 3) * 32, 16, 1024);
-                    umma_bf16(tmem + sb * C::BN, da, db, idS, kk > 0 ? 1u : 0u);
-                }
+                for (int kk = 1; kk < D / 16; ++kk) umma_ss<1>(sd, dQ[kk], dK[kk], idS);
                 umma_commit(&bars->s_full[sb]);
                 umma_commit_mc(&bars->kv_empty[slot], mc_mask);
                 if (jj >= 1) issue_pv(jj - 1);
