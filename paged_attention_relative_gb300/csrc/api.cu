@@ -95,13 +95,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // rel_logits (T, H, R) as a 3-D TMA tensor, innermost first: (R, H, T), box
-// (144 distances, G heads, ts tokens), no swizzle; needs R % 8 == 0.
+// (prefill_bias_window() distances, G heads, ts tokens), no swizzle; needs
+// R % 8 == 0.
 rel_attn_status make_rel_map(const rel_attn_tensor* t, int G, int ts, CUtensorMap* map) {
     auto enc = encode_fn();
     if (!enc) return fail(REL_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t dims[3] = {(cuuint64_t)t->shape[2], (cuuint64_t)t->shape[1], (cuuint64_t)t->shape[0]};
     cuuint64_t strides[2] = {(cuuint64_t)t->stride[1] * 2, (cuuint64_t)t->stride[0] * 2};
-    cuuint32_t box[3] = {144, (cuuint32_t)G, (cuuint32_t)ts};
+    cuuint32_t box[3] = {(cuuint32_t)prefill_bias_window(), (cuuint32_t)G, (cuuint32_t)ts};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, t->data, dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -58,8 +58,11 @@ cudaError_t launch_decode(const AttnParams& p, const LaunchShape& shape, cudaStr
 // tcgen05 prefill kernel for 128-row GQA-packed query tiles.  maps[0] / maps[1]
 // describe key_cache / value_cache as 4-D TMA tensors (D, Hk, BS, NB) with a
 // (64, 1, 16, 1) box and 128-byte swizzle; maps[2] describes rel_logits as a
-// 3-D tensor (R, H, T) with a (144, G, bias_ts) box (only read when vec_bias).
+// 3-D tensor (R, H, T) with a (prefill_bias_window(), G, bias_ts) box (only
+// read when vec_bias).
 LaunchShape prefill_shape(const AttnParams& p);
+// rel_logits values per staged bias row (the inner box extent of maps[2]).
+int prefill_bias_window();
 cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap* maps, const LaunchShape& shape,
                            cudaStream_t stream);
 

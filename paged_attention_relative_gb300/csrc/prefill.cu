@@ -743,6 +743,8 @@ cudaError_t launch_t(const AttnParams& p, const CUtensorMap* maps, const LaunchS
 
 }  // namespace
 
+int prefill_bias_window() { return PrefillCfg<128>::kBiasW; }
+
 LaunchShape prefill_shape(const AttnParams& p) {
     LaunchShape s;
     const int tpt = 128 / p.G;
