@@ -81,7 +81,10 @@ struct PrefillCfg {
     static constexpr int kThreads = 384;
     static constexpr int kStages = D == 128 ? 4 : 8;  // K/V tile slots: a K ring, then a V ring
     static constexpr int kRing = kStages / 2;
-    static constexpr int kBiasW = 144;                // rel_logits values per staged bias row
+    // rel_logits values per staged bias row: at least 128 + 14 (a tile plus the
+    // shear of an 8-token sub-box and 16-byte alignment); 152 makes the row
+    // pitch 76 words, so the 32 rows of a warp spread over the banks.
+    static constexpr int kBiasW = 152;
     // 128 rows, plus up to 16 token sub-boxes each padded to a 128-byte boundary
     static constexpr int kBiasBytes = 128 * kBiasW * 2 + 16 * 128;
     static constexpr int kXchBytes = 3 * 2 * 128 * 4;  // half-row maxima (2 buffers), half-row sums
@@ -503,9 +506,15 @@ __global__ void __launch_bounds__(384, 1)
         const int sub_bytes = (TS * G * C::kBiasW * 2 + 127) & ~127;  // TMA destinations are 128-byte aligned
         const int i_sub = (i_rel / TS) * TS;
         const int e_r = (i_rel - i_sub) + ((i0 + i_sub + off - 127) & 7);
-        const uint16_t* win = reinterpret_cast<const uint16_t*>(sBias + (i_rel / TS) * sub_bytes +
-                                                                (r - i_sub * G) * (C::kBiasW * 2)) +
-                              e_r + 127 - kh;
+        // This half's 64 keys read elements base_h - k (k = 0..63), i.e. the
+        // 32-bit words W0 - 31 .. W0 + 1 of the row; key pair (2m, 2m+1) sits
+        // in word W0 - m, or straddles words W0 - m and W0 - m + 1 when
+        // base_h is even (one byte permute either way).
+        const int base_h = e_r + 127 - kh;
+        const uint32_t* wrow = reinterpret_cast<const uint32_t*>(sBias + (i_rel / TS) * sub_bytes +
+                                                                 (r - i_sub * G) * (C::kBiasW * 2)) +
+                               (((base_h - 1) >> 1) - 31);
+        const uint32_t psel = ((base_h - 1) & 1) ? 0x5432u : 0x3210u;
         int nb = 0;  // band tiles consumed
 
         for (int jj = 0; jj < n_it; ++jj) {
@@ -542,11 +551,15 @@ __global__ void __launch_bounds__(384, 1)
                         if constexpr (VEC) {
                             if (!mbar_wait(&bars->bias_full, nb & 1, p.timeout_ns, kSitePrefillRelFull, p.err))
                                 bars->abort = 1;
+                            uint32_t wv[33];
 #pragma unroll
-                            for (int e = 0; e < 32; ++e)
+                            for (int i = 0; i < 33; ++i) wv[i] = wrow[i];
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) {
+                                const uint32_t pr = __byte_perm(wv[31 - e], wv[32 - e], psel);
                                 s[e] = __ffma2_rn(s[e], sc2,
-                                                  make_float2(bf16_bits_to_f32(win[-2 * e]),
-                                                              bf16_bits_to_f32(win[-2 * e - 1])));
+                                                  make_float2(__uint_as_float(pr & 0xffff0000u), __uint_as_float(pr << 16)));
+                            }
                             // Every read of this band tile's windows is done.
                             __syncwarp();
                             if (lane == 0) mbar_arrive(&bars->bias_empty);
