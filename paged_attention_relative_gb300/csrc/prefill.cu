@@ -8,9 +8,8 @@
 // and the bias band come first, so the running maximum settles early).
 //
 // Warp roles (384 threads):
-//   warps 0, 2 producers: warp 0 loads Q once with 16-byte cp.async
-//              (GQA-packed rows), then the K tiles; warp 2 the V tiles, each
-//              into its own ring so K never waits behind a V slot.  A tile
+//   warps 0, 2 producers: warp 0 loads the K tiles, warp 2 the V tiles,
+//              each into its own ring so K never waits behind a V slot.  A tile
 //              arrives as 2 KB TMA boxes (16 keys x 64 dims) straight from the
 //              paged cache, one per fully visible 16-key group, multicast to
 //              the other CTA of the cluster (the two take turns issuing), with
@@ -24,9 +23,10 @@
 //              bias band) it stages that tile's rel_logits by TMA once the
 //              softmax warps have read the previous band tile's (see below).
 //   warp 3     MMA issuer (one thread) and TMEM owner: S_j = Q K_j^T into one
-//              of two TMEM buffers (M=128, N=128, K=head_dim), then
-//              O += P_{j-1} V_{j-1} with P read from TMEM and V from shared
-//              memory (MN-major); tcgen05.commit signals completion.
+//              of two TMEM buffers (M=128, N=128, K=head_dim, Q read from
+//              TMEM), then O += P_{j-1} V_{j-1} with P read from TMEM and V
+//              from shared memory (MN-major); tcgen05.commit signals
+//              completion.
 //   warps 4-11 softmax: warps 4-7 take keys [0, 64) of every tile and warps
 //              8-11 keys [64, 128); warp w reads TMEM lanes 32*(w%4).. so
 //              thread (w, lane) owns half of row 32*(w%4) + lane.  Per tile it
@@ -48,9 +48,11 @@
 // Every mbarrier wait is bounded; on timeout the kernel records the site in
 // the device error word and winds down.
 //
-// TMEM columns: S0 [0,128), S1 [128,256), O [256,256+D), P0 [384,448),
-// P1 [448,512); within S and P the first half of the columns holds keys
-// [0, 64) of the tile.
+// TMEM columns: S0 [0,128), S1 [128,256), O [256,256+D), Q [256+D,256+3D/2).
+// P_j overwrites the first half of each 64-column half of S_j's buffer once
+// the thread owning that half has read it (keys [0, 64) of the tile in
+// columns [0, 32), keys [64, 128) in [64, 96)).  Warps 4-7 copy Q into TMEM
+// at the start.
 //
 // Semantics: vLLM API docs, inkling_fa4_rel_attention (paged varlen forward);
 // bias rule: prhub report on vLLM PR #48858, score_mod_rel_bias.
@@ -75,12 +77,13 @@ struct PrefillCfg {
     static constexpr int BN = 128;                  // keys per tile (query tiles are 128 rows)
     static constexpr int kDB = D / 64;              // 64-dim (128-byte) column blocks
     static constexpr int kBlk = 128 * 128;          // one 128-row x 128-byte block
-    static constexpr int kTileBytes = kDB * kBlk;   // a Q, K or V tile
+    static constexpr int kTileBytes = kDB * kBlk;   // a K or V tile
     static constexpr int kMmaWarp = 3;
     static constexpr int kSoftThreads = 256;        // warps 4-11
     static constexpr int kThreads = 384;
-    static constexpr int kStages = D == 128 ? 4 : 8;  // K/V tile slots: a K ring, then a V ring
-    static constexpr int kRing = kStages / 2;
+    static constexpr int kKRing = D == 128 ? 3 : 6;   // K tile slots
+    static constexpr int kVRing = D == 128 ? 2 : 4;   // V tile slots (after the K ring)
+    static constexpr int kStages = kKRing + kVRing;
     // rel_logits values per staged bias row: at least 128 + 14 (a tile plus the
     // shear of an 8-token sub-box and 16-byte alignment); 152 makes the row
     // pitch 76 words, so the 32 rows of a warp spread over the banks.
@@ -88,20 +91,18 @@ struct PrefillCfg {
     // 128 rows, plus up to 16 token sub-boxes each padded to a 128-byte boundary
     static constexpr int kBiasBytes = 128 * kBiasW * 2 + 16 * 128;
     static constexpr int kXchBytes = 3 * 2 * 128 * 4;  // half-row maxima (2 buffers), half-row sums
-    static constexpr int kData = kTileBytes + kStages * kTileBytes + kBiasBytes + kXchBytes;
+    static constexpr int kData = kStages * kTileBytes + kBiasBytes + kXchBytes;
     static constexpr int kTmemCols = 512;
-    static constexpr int kOCol = 256;
-    static constexpr int kPCol = 384;  // + 64 * buffer
+    static constexpr int kOCol = 256;      // O: D columns
+    static constexpr int kQCol = 256 + D;  // Q: D / 2 columns (bf16 pairs)
 };
 
 struct PrefillBars {
     uint64_t q_full;
-    uint64_t kv_full[8];
-    uint64_t kv_empty[8];
+    uint64_t kv_full[10];
+    uint64_t kv_empty[10];
     uint64_t s_full[2];
-    uint64_t s_empty[2];
     uint64_t p_full[2];
-    uint64_t p_free[2];
     uint64_t o_done;   // one phase per PV tile (rescale waits, never more than one phase behind)
     uint64_t o_final;  // single phase: every MMA of the CTA has completed
     uint64_t bias_full;   // one phase per band tile: its rel_logits windows have landed
@@ -125,8 +126,7 @@ __global__ void __launch_bounds__(384, 1)
     using C = PrefillCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sQ = smem;
-    uint8_t* sKV = smem + C::kTileBytes;
+    uint8_t* sKV = smem;
     uint8_t* sBias = sKV + C::kStages * C::kTileBytes;
     float* sXch = reinterpret_cast<float*>(sBias + C::kBiasBytes);  // [3 bufs][2 halves][128 rows]
     PrefillBars* bars = reinterpret_cast<PrefillBars*>(sBias + C::kBiasBytes + C::kXchBytes);
@@ -190,16 +190,14 @@ __global__ void __launch_bounds__(384, 1)
     auto band_tile = [&](int j0) { return R > 0 && pos_max - j0 >= 0 && pos_min - (j0 + C::BN - 1) < R; };
 
     if (threadIdx.x == 0) {
-        mbar_init(&bars->q_full, 32);
+        mbar_init(&bars->q_full, C::kSoftThreads / 2);
         for (int i = 0; i < C::kStages; ++i) {
             mbar_init(&bars->kv_full[i], 33);  // producer lanes + the expect_tx arrival
             mbar_init(&bars->kv_empty[i], n_act);  // one MMA commit per active CTA of the cluster
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->s_full[i], 1);
-            mbar_init(&bars->s_empty[i], C::kSoftThreads);
             mbar_init(&bars->p_full[i], C::kSoftThreads);
-            mbar_init(&bars->p_free[i], 1);
         }
         mbar_init(&bars->o_done, 1);
         mbar_init(&bars->o_final, 1);
@@ -243,11 +241,9 @@ __global__ void __launch_bounds__(384, 1)
         constexpr int kRows = 32 / kChunks;
         constexpr int kPerPage = 16 / kRows;
         const int lrow = lane / kChunks, lchunk = lane % kChunks;
-        const uint16_t* qg = reinterpret_cast<const uint16_t*>(p.q);
         const uint16_t* cache = reinterpret_cast<const uint16_t*>(is_v ? p.v_cache : p.k_cache);
         const CUtensorMap* tmap = is_v ? &tm_v : &tm_k;
         const int32_t* bt = p.block_table + (size_t)b * p.bt_stride;
-        const uint64_t pol_first = l2_policy_evict_first();
         const uint64_t pol_last = l2_policy_evict_last();
         const uint32_t col_off = (lchunk >> 3) * C::kBlk;
         // Within a 16-row group, row (kk*kRows + lrow) & 7 == ((kk*kRows) & 7) | lrow,
@@ -257,28 +253,11 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t cx = (uint32_t)((lchunk & 7) ^ lrow);
         const uint32_t dst_lane = col_off + lrow * 128;
         if (lane == 0) tma_prefetch_desc(tmap);
-        // At most one cp.async group is in flight: the Q tile, then the
-        // partial groups of a stage.  It is retired (landed, proxy-fenced,
-        // one arrival per lane) after the next stage has been issued, or
-        // before the producer blocks on a full ring.
+        // At most one cp.async group (the partial groups of a tile) is in
+        // flight; it is retired (landed, proxy-fenced, one arrival per lane)
+        // after the next tile has been issued, or before the producer blocks
+        // on a full ring.
         uint64_t* pend = nullptr;
-        if (!is_v) {
-            for (int pg = 0; pg < 8; ++pg) {
-#pragma unroll
-                for (int kk = 0; kk < kPerPage; ++kk) {
-                    const int r = 16 * pg + kk * kRows + lrow;
-                    const bool valid = r < n_rows;
-                    const int tok = i0 + r / G, hh = r % G;
-                    const uint16_t* src =
-                        qg + (size_t)(q0 + tok) * p.q_st + (size_t)(g * G + hh) * p.q_sh + lchunk * 8;
-                    const uint32_t dst =
-                        smem_u32(sQ) + dst_lane + (16 * pg + kk * kRows) * 128 + ((cx ^ ((kk * kRows) & 7)) << 4);
-                    cp_async_16(dst, valid ? src : qg, valid ? 16u : 0u, pol_first);
-                }
-            }
-            cp_async_commit();
-            pend = &bars->q_full;
-        }
         auto retire = [&](int newer) {
             cp_async_wait(newer);
             fence_proxy_async_smem();
@@ -298,10 +277,11 @@ __global__ void __launch_bounds__(384, 1)
         int bt_cur = load_bt(0), bt_n1 = load_bt(1), bt_n2 = load_bt(2);
         // TMA lanes: lane -> (16-key group lane / kDB, 64-dim block lane % kDB).
         const int t_pg = lane / C::kDB, t_db = lane % C::kDB;
-        const int ring0 = is_v ? C::kRing : 0;
+        const int ring0 = is_v ? C::kKRing : 0;
+        const int ring = is_v ? C::kVRing : C::kKRing;
         for (int jj = 0; jj < n_it; ++jj) {
-            const int slot = ring0 + jj % C::kRing;
-            const int round = jj / C::kRing;
+            const int slot = ring0 + jj % ring;
+            const int round = jj / ring;
             // Never block on a full ring while holding copies whose landing has
             // not been signalled: the consumer may be waiting for exactly those.
             if (!mbar_try_wait(&bars->kv_empty[slot], (round & 1) ^ 1)) {
@@ -364,9 +344,9 @@ __global__ void __launch_bounds__(384, 1)
         // Wait until every active CTA has released each slot for the last
         // time: afterwards no peer commit is still travelling to this CTA.
         if (!__any_sync(0xffffffffu, aborted(bars))) {
-            for (int i = 0; i < min(C::kRing, n_it); ++i) {
-                const int last = i + C::kRing * ((n_it - 1 - i) / C::kRing);
-                if (!mbar_wait(&bars->kv_empty[ring0 + i], (last / C::kRing) & 1, p.timeout_ns,
+            for (int i = 0; i < min(ring, n_it); ++i) {
+                const int last = i + ring * ((n_it - 1 - i) / ring);
+                if (!mbar_wait(&bars->kv_empty[ring0 + i], (last / ring) & 1, p.timeout_ns,
                                kSitePrefillKEmpty, p.err))
                     bars->abort = 1;
             }
@@ -408,28 +388,30 @@ __global__ void __launch_bounds__(384, 1)
         if (lane == 0 && n_it > 0) {
             constexpr uint32_t idS = umma_idesc_bf16(128, C::BN, false);
             constexpr uint32_t idPV = umma_idesc_bf16(128, D, true);
-            const uint32_t aQ = smem_u32(sQ), aKV = smem_u32(sKV);
+            const uint32_t aKV = smem_u32(sKV);
             bool ok = mbar_wait(&bars->q_full, 0, p.timeout_ns, kSitePrefillLoadQ, p.err);
             // Descriptors are formed before each wait, so the MMAs of a tile
             // issue back to back (any instruction between two of them delays
             // the tensor pipe).  A descriptor's low bits hold address / 16, so
             // a byte offset inside shared memory adds offset / 16.
-            uint64_t dQ[D / 16];
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) dQ[kk] = umma_desc_sw128(aQ + (kk >> 2) * C::kBlk + (kk & 3) * 32, 16, 1024);
             const uint64_t dK0 = umma_desc_sw128(aKV, 16, 1024);
             const uint64_t dV0 = umma_desc_sw128(aKV, C::kBlk, 1024);
+            const uint32_t aq = tmem + C::kQCol;
+            // P_t sits in S buffer t % 2: keys [64h, 64h + 64) in columns
+            // [64h, 64h + 32) of the buffer.  The MMAs of this thread run in
+            // issue order, so S_{t+2} = Q K^T, issued after PV_t, overwrites
+            // the buffer only once PV_t has read P_t.
             auto issue_pv = [&](int t) {
                 const int pb = t & 1;
-                const int slot = C::kRing + t % C::kRing;
+                const int slot = C::kKRing + t % C::kVRing;
                 const uint64_t dv = dV0 + (uint64_t)((slot * C::kTileBytes) >> 4);
                 uint64_t dV[C::BN / 16];
 #pragma unroll
                 for (int kk = 0; kk < C::BN / 16; ++kk) dV[kk] = dv + (uint64_t)((kk * 16 * 128) >> 4);
-                const uint32_t pcol = tmem + C::kPCol + 64 * pb;
+                const uint32_t pcol = tmem + pb * C::BN;
                 const uint32_t od = tmem + C::kOCol;
                 ok = ok && mbar_wait(&bars->p_full[pb], (t >> 1) & 1, p.timeout_ns, kSitePrefillPFull, p.err);
-                ok = ok && mbar_wait(&bars->kv_full[slot], (t / C::kRing) & 1, p.timeout_ns, kSitePrefillVFull,
+                ok = ok && mbar_wait(&bars->kv_full[slot], (t / C::kVRing) & 1, p.timeout_ns, kSitePrefillVFull,
                                      p.err);
                 if (!ok) return;
                 tc_fence_after();
@@ -438,28 +420,26 @@ __global__ void __launch_bounds__(384, 1)
                 else
                     umma_ts<0>(od, pcol, dV[0], idPV);
 #pragma unroll
-                for (int kk = 1; kk < C::BN / 16; ++kk) umma_ts<1>(od, pcol + kk * 8, dV[kk], idPV);
+                for (int kk = 1; kk < C::BN / 16; ++kk)
+                    umma_ts<1>(od, pcol + 64 * (kk >> 2) + 8 * (kk & 3), dV[kk], idPV);
                 umma_commit(&bars->o_done);
                 umma_commit_mc(&bars->kv_empty[slot], mc_mask);
-                umma_commit(&bars->p_free[pb]);
             };
             for (int jj = 0; jj < n_it && ok; ++jj) {
                 const int sb = jj & 1;
-                const int slot = jj % C::kRing;
+                const int slot = jj % C::kKRing;
                 const uint64_t dk = dK0 + (uint64_t)((slot * C::kTileBytes) >> 4);
                 uint64_t dK[D / 16];
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) dK[kk] = dk + (uint64_t)((((kk >> 2) * C::kBlk) + (kk & 3) * 32) >> 4);
                 const uint32_t sd = tmem + sb * C::BN;
-                ok = ok && mbar_wait(&bars->kv_full[slot], (jj / C::kRing) & 1, p.timeout_ns, kSitePrefillKFull,
-                                     p.err);
-                ok = ok && mbar_wait(&bars->s_empty[sb], ((jj >> 1) & 1) ^ 1, p.timeout_ns, kSitePrefillSEmpty,
+                ok = ok && mbar_wait(&bars->kv_full[slot], (jj / C::kKRing) & 1, p.timeout_ns, kSitePrefillKFull,
                                      p.err);
                 if (!ok) break;
                 tc_fence_after();
-                umma_ss<0>(sd, dQ[0], dK[0], idS);
+                umma_ts<0>(sd, aq, dK[0], idS);
 #pragma unroll
-                for (int kk = 1; kk < D / 16; ++kk) umma_ss<1>(sd, dQ[kk], dK[kk], idS);
+                for (int kk = 1; kk < D / 16; ++kk) umma_ts<1>(sd, aq + 8 * kk, dK[kk], idS);
                 umma_commit(&bars->s_full[sb]);
                 umma_commit_mc(&bars->kv_empty[slot], mc_mask);
                 if (jj >= 1) issue_pv(jj - 1);
@@ -496,6 +476,27 @@ __global__ void __launch_bounds__(384, 1)
         const int kh = 64 * half;  // first key of this half within a tile
         float m_run = -CUDART_INF_F, l_half = 0.f;
         bool any_abort = false;
+
+        // Warps 4-7 copy the Q tile into TMEM: row r to lane r, bf16 pairs per
+        // column (zeros past the tile's rows).
+        if (half == 0) {
+            uint32_t qv[D / 64][32];
+            const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.q) +
+                                                              (size_t)t * p.q_st + (size_t)h * p.q_sh);
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) {
+                const uint4 v = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+                qv[c / 8][4 * (c % 8)] = v.x;
+                qv[c / 8][4 * (c % 8) + 1] = v.y;
+                qv[c / 8][4 * (c % 8) + 2] = v.z;
+                qv[c / 8][4 * (c % 8) + 3] = v.w;
+            }
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) tmem_st32(lane_base + C::kQCol + 32 * c, qv[c]);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&bars->q_full);
+        }
 
         // Bias windows (VEC): a band tile's rel_logits arrive by TMA as rows of
         // kBiasW values, one row per (token, head) of the tile, each starting at
@@ -543,7 +544,6 @@ __global__ void __launch_bounds__(384, 1)
                     }
                 }
                 tc_fence_before();
-                mbar_arrive(&bars->s_empty[sb]);
 
                 if (!raw) {
                     const float2 sc2 = make_float2(sc, sc);
@@ -620,9 +620,8 @@ __global__ void __launch_bounds__(384, 1)
             const float alpha = grow ? ex2((m_run - m_use) * kLog2e) : 1.f;
             const float c1 = raw ? sl2 : kLog2e;
 
-            // This half of P_j into TMEM buffer jj % 2 once PV_{j-2} has read it.
-            if (!mbar_wait(&bars->p_free[sb], ((jj >> 1) & 1) ^ 1, p.timeout_ns, kSitePrefillPFull, p.err))
-                bars->abort = 1;
+            // This half of P_j over the S columns this thread has already read
+            // (PV_{j-2}, the last reader of the buffer, completed before S_j).
             float2 rs[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) rs[i] = make_float2(0.f, 0.f);
@@ -636,7 +635,7 @@ __global__ void __launch_bounds__(384, 1)
                     rs[e & 3] = __fadd2_rn(rs[e & 3], pe);
                     w[e] = pack_bf16(pe.x, pe.y);
                 }
-                tmem_st32(lane_base + C::kPCol + 64 * sb + 32 * half, w);
+                tmem_st32(lane_base + sb * C::BN + kh, w);
             }
             const float2 rs2 = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
             l_half = l_half * alpha + (rs2.x + rs2.y);
