@@ -22,6 +22,7 @@ enum WaitSite : int {
     kSitePrefillRelFull = 18,
     kSitePrefillRelEmpty = 19,
     kSitePrefillSEmpty = 20,
+    kSitePrefillXchg = 21,
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -90,7 +90,7 @@ struct PrefillCfg {
     static constexpr int kBiasW = 152;
     // 128 rows, plus up to 16 token sub-boxes each padded to a 128-byte boundary
     static constexpr int kBiasBytes = 128 * kBiasW * 2 + 16 * 128;
-    static constexpr int kXchBytes = 3 * 2 * 128 * 4;  // half-row maxima (2 buffers), half-row sums
+    static constexpr int kXchBytes = 3 * 2 * 128 * 4;  // half-row maxima (2 tile buffers), half-row sums
     static constexpr int kData = kStages * kTileBytes + kBiasBytes + kXchBytes;
     static constexpr int kTmemCols = 512;
     static constexpr int kOCol = 256;      // O: D columns
@@ -103,6 +103,7 @@ struct PrefillBars {
     uint64_t kv_empty[10];
     uint64_t s_full[2];
     uint64_t p_full[2];
+    uint64_t x_full[2];      // per tile parity: every softmax warp has published its half-row maxima
     uint64_t o_done;   // one phase per PV tile (rescale waits, never more than one phase behind)
     uint64_t o_final;  // single phase: every MMA of the CTA has completed
     uint64_t bias_full;   // one phase per band tile: its rel_logits windows have landed
@@ -198,6 +199,7 @@ __global__ void __launch_bounds__(384, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->s_full[i], 1);
             mbar_init(&bars->p_full[i], C::kSoftThreads);
+            mbar_init(&bars->x_full[i], C::kSoftThreads / 32);
         }
         mbar_init(&bars->o_done, 1);
         mbar_init(&bars->o_final, 1);
@@ -602,32 +604,34 @@ __global__ void __launch_bounds__(384, 1)
                 mx = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]), fmaxf(mk[6], mk[7]));
                 if (raw) mx *= sc;
             }
-            // Exchange the half-row maxima (and the abort decision) with the partner half.
-            sXch[((sb * 2) + half) * 128 + r] = mx;
-            if (bar_or(1, C::kSoftThreads, my_abort)) {
+            if (my_abort) {
                 any_abort = true;
                 break;
             }
-            mx = fmaxf(mx, sXch[((sb * 2) + (half ^ 1)) * 128 + r]);
             if (band) ++nb;
-            // Lazy rescaling: the reference maximum m_run only moves when the
-            // row maximum exceeds it by more than 8 in log2 units, so P stays
-            // below 2^8 and O is rescaled rarely; O / l is unchanged.
-            const float m_tile = fmaxf(m_run, mx);
-            const bool grow = m_run != -CUDART_INF_F && m_tile > m_run + kLazyRescale;
-            const float m_use = (m_run == -CUDART_INF_F || grow) ? m_tile : m_run;
-            const float ml = m_use == -CUDART_INF_F ? 0.f : m_use * kLog2e;
-            const float alpha = grow ? ex2((m_run - m_use) * kLog2e) : 1.f;
+            // Publish this half's maximum.  The partner's is needed only to
+            // confirm the reference maximum (or, before the first visible
+            // key, to set it), so the exponentials start from the current
+            // reference and are redone in the rare case that it moves.
+            const int xb = jj & 1;
+            sXch[(xb * 2 + half) * 128 + r] = mx;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->x_full[xb]);
+            auto row_max = [&]() -> float {
+                if (!mbar_wait(&bars->x_full[xb], (jj >> 1) & 1, p.timeout_ns, kSitePrefillXchg, p.err))
+                    bars->abort = 1;
+                return fmaxf(mx, sXch[(xb * 2 + (half ^ 1)) * 128 + r]);
+            };
             const float c1 = raw ? sl2 : kLog2e;
-
-            // This half of P_j over the S columns this thread has already read
-            // (PV_{j-2}, the last reader of the buffer, completed before S_j).
-            float2 rs[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) rs[i] = make_float2(0.f, 0.f);
-            {
+            uint32_t w[32];
+            float rsum = 0.f;
+            // This half of P_j (bf16 pairs) and its row sum against reference m.
+            auto exp_pass = [&](float m) {
+                const float ml = m == -CUDART_INF_F ? 0.f : m * kLog2e;
                 const float2 c12 = make_float2(c1, c1), nml = make_float2(-ml, -ml);
-                uint32_t w[32];
+                float2 rs[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) rs[i] = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const float2 x = __ffma2_rn(s[e], c12, nml);
@@ -635,10 +639,31 @@ __global__ void __launch_bounds__(384, 1)
                     rs[e & 3] = __fadd2_rn(rs[e & 3], pe);
                     w[e] = pack_bf16(pe.x, pe.y);
                 }
-                tmem_st32(lane_base + sb * C::BN + kh, w);
+                const float2 rs2 = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
+                rsum = rs2.x + rs2.y;
+            };
+            // Lazy rescaling: the reference maximum m_run only moves when the
+            // row maximum exceeds it by more than 8 in log2 units, so P stays
+            // below 2^8 and O is rescaled rarely; O / l is unchanged.
+            float m_use = m_run;
+            bool grow = false;
+            if (m_run == -CUDART_INF_F) {
+                m_use = row_max();
+                exp_pass(m_use);
+            } else {
+                exp_pass(m_run);
+                const float rmx = row_max();
+                if (rmx > m_run + kLazyRescale) {
+                    grow = true;
+                    m_use = rmx;
+                    exp_pass(m_use);
+                }
             }
-            const float2 rs2 = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
-            l_half = l_half * alpha + (rs2.x + rs2.y);
+            const float alpha = grow ? ex2((m_run - m_use) * kLog2e) : 1.f;
+            // This half of P_j over the S columns this thread has already read
+            // (PV_{j-2}, the last reader of the buffer, completed before S_j).
+            tmem_st32(lane_base + sb * C::BN + kh, w);
+            l_half = l_half * alpha + rsum;
             m_run = m_use;
 
             // Rescale this half of the O row when the reference maximum moved
