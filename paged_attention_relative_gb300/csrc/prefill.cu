@@ -3,9 +3,11 @@
 // One CTA per (128-row query tile, kv head, request, split).  Rows are
 // GQA-packed token-major: row r of the tile is query token i0 + r / G of
 // request b and query head g*G + r % G, so every K/V tile read for kv head g
-// serves all G query heads.  The visible key range of the tile is cut into
-// 128-key tiles, processed from the last to the first (the causal diagonal
-// and the bias band come first, so the running maximum settles early).
+// serves all G query heads.  CTAs run in clusters of two adjacent query
+// tiles that walk one sequence of 128-key tiles (the union of their visible
+// ranges, processed from the last to the first: the causal diagonal and the
+// bias band come first, so the running maximum settles early) and receive
+// every K/V tile through TMA multicast.
 //
 // Warp roles (384 threads):
 //   warps 0, 2 producers: warp 0 loads the K tiles, warp 2 the V tiles,
@@ -33,18 +35,18 @@
 //              reads its half of S_j, forms sc * q.k + bias (natural units;
 //              tiles outside every row's bias band keep the raw q.k and fold
 //              the scale into the exponent), masks only when some row of the
-//              warp does not see the whole half tile, exchanges the half-row
-//              maximum with its partner through shared memory (one named
-//              barrier per tile), keeps the fp32 online softmax, writes its
-//              half of P_j into TMEM as bf16 pairs, rescales its half of the O
-//              row when the row maximum grew, and writes its half of the
-//              output.  The reference maximum moves lazily (only when the
-//              row maximum exceeds it by more than 2^8), so O is rarely
-//              rescaled.  The bias of a band tile is staged by warp 1:
-//              one 144-value window per (token, head) row, starting at the
-//              16-byte aligned distance below the row's token sub-box, zero
-//              outside [0, R), so the sheared gather becomes a reversed
-//              shared-memory read.
+//              warp does not see the whole half tile, publishes its half-row
+//              maximum to its partner through shared memory (an mbarrier per
+//              tile parity), computes its half of P_j against the current
+//              reference maximum while the partner's arrives, writes it into
+//              TMEM as bf16 pairs, rescales its half of the O row when the
+//              reference moved, and writes its half of the output.  The
+//              reference maximum moves lazily (only when the row maximum
+//              exceeds it by more than 2^8), so O is rarely rescaled.  The
+//              bias of a band tile is staged by warp 1: one 152-value window
+//              per (token, head) row, starting at the 16-byte aligned
+//              distance below the row's token sub-box, zero outside [0, R),
+//              so the sheared gather becomes a reversed shared-memory read.
 // Every mbarrier wait is bounded; on timeout the kernel records the site in
 // the device error word and winds down.
 //
@@ -566,7 +568,7 @@ __global__ void __launch_bounds__(384, 1)
                             __syncwarp();
                             if (lane == 0) mbar_arrive(&bars->bias_empty);
                         } else {
-#pragma unroll 4
+#pragma unroll
                             for (int e = 0; e < 32; ++e) {
                                 const int d = pos - (jh + 2 * e);
                                 const float b0 =
