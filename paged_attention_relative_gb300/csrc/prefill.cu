@@ -192,6 +192,10 @@ __global__ void __launch_bounds__(384, 1)
     constexpr bool vec_bias = VEC;
     auto band_tile = [&](int j0) { return R > 0 && pos_max - j0 >= 0 && pos_min - (j0 + C::BN - 1) < R; };
 
+    // A cluster with no rows at all touches no shared memory of another CTA:
+    // both of its CTAs leave at once (the same test in both).
+    if (active == 0) return;
+
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, C::kSoftThreads / 2);
         for (int i = 0; i < C::kStages; ++i) {
