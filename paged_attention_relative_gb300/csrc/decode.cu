@@ -50,6 +50,8 @@ struct DecodeCfg {
     static constexpr int kMaxStages = 12;
 };
 
+constexpr int kRankMax = 256;
+
 template <int D, int MT, int KSL>
 __global__ void __launch_bounds__(DecodeCfg<D, MT, KSL>::kMaxThreads) decode_kernel(const AttnParams p) {
     using C = DecodeCfg<D, MT, KSL>;
@@ -63,8 +65,29 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, KSL>::kMaxThreads) decode_ker
     int* abort_flag = reinterpret_cast<int*>(empty + C::kMaxStages);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int split = blockIdx.x, g = blockIdx.y;
     const int G = p.G;
+
+    // Longest requests first: grid index z takes the request of rank z in
+    // decreasing cache length (ties by index), so the longest streams start
+    // in the first wave and the short ones fill in behind them.  Ranking costs
+    // B^2 comparisons per CTA, so only batches of up to kRankMax requests.
+    int b = blockIdx.z;
+    if (p.B > 1 && p.B <= kRankMax) {
+        int* chosen = abort_flag + 1;
+        const int target = blockIdx.z;
+        for (int c = threadIdx.x; c < p.B; c += blockDim.x) {
+            const int lc = p.cache_seqlens[c];
+            int rank = 0;
+            for (int o = 0; o < p.B; ++o) {
+                const int lo_ = p.cache_seqlens[o];
+                rank += (lo_ > lc) || (lo_ == lc && o < c);
+            }
+            if (rank == target) *chosen = c;
+        }
+        __syncthreads();
+        b = *chosen;
+    }
 
     const int q0 = p.cu_seqlens_q[b];
     const int sq = p.cu_seqlens_q[b + 1] - q0;
@@ -423,7 +446,7 @@ int pick_stages(int ctas, int num_sms) {
     using C = DecodeCfg<D, MT, KSL>;
     // One CTA per SM when the grid fits in one wave, else two per SM; the
     // ring takes what shared memory allows so the producer runs far ahead.
-    const int budget = (ctas <= num_sms) ? 224 * 1024 : 111 * 1024;
+    const int budget = (ctas <= num_sms || KSL == 8) ? 224 * 1024 : 111 * 1024;
     int n = (budget - 512) / C::kStageBytes;
     if (n > C::kMaxStages) n = C::kMaxStages;
     if (n < 2) n = 2;
@@ -449,7 +472,11 @@ LaunchShape decode_shape(const AttnParams& p, int num_sms) {
     const int ctas = p.num_splits * p.Hk * p.B;
     if (p.max_rows <= 16) {
         s.mt = 1;
-        s.ksl = ctas <= num_sms ? 8 : 4;
+        // Eight consumer warps and four producers, one CTA per SM: one CTA
+        // streams its (request, kv head) at close to an SM's share of HBM
+        // bandwidth, and with the longest requests first the grid's tail is
+        // the short ones.
+        s.ksl = 8;
     } else if (p.max_rows <= 32) {
         s.mt = 2;
         s.ksl = 4;
