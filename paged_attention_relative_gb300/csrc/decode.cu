@@ -444,8 +444,9 @@ int decode_smem_bytes(int nst) {
 template <int D, int MT, int KSL>
 int pick_stages(int ctas, int num_sms) {
     using C = DecodeCfg<D, MT, KSL>;
-    // One CTA per SM when the grid fits in one wave, else two per SM; the
-    // ring takes what shared memory allows so the producer runs far ahead.
+    // One CTA per SM when the grid fits in one wave or the CTA has eight
+    // consumer warps, else two per SM; the ring takes what shared memory
+    // allows so the producers run far ahead.
     const int budget = (ctas <= num_sms || KSL == 8) ? 224 * 1024 : 111 * 1024;
     int n = (budget - 512) / C::kStageBytes;
     if (n > C::kMaxStages) n = C::kMaxStages;
