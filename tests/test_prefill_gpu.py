@@ -42,6 +42,12 @@ SMALL = [
          num_kv_heads=2, head_dim=128),
     dict(name="block32", seqlens_q=[33], seqlens_k=[333], num_heads=8, num_kv_heads=2, head_dim=128,
          block_size=32),
+    # four tokens per tile: one bias box holds all 32 heads of a 4-token sub-box
+    dict(name="gqa32_four_tokens_per_tile", seqlens_q=[11, 6], seqlens_k=[400, 6], num_heads=64,
+         num_kv_heads=2, head_dim=128, rel_extent=96),
+    # one token per tile (every row of a tile is a head of the same token)
+    dict(name="gqa128_one_token_per_tile", seqlens_q=[3, 2], seqlens_k=[260, 70], num_heads=128,
+         num_kv_heads=1, head_dim=64, rel_extent=40),
 ]
 
 
