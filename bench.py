@@ -305,20 +305,20 @@ def time_oracle(case, budget_s: float):
     T, H = d["T"], d["H"]
     n_rows = T * H
     rng = np.random.default_rng(0)
-    # Probe with a few rows, then size the sample to the budget.
-    probe = min(n_rows, max(cores, 8))
-    idx = rng.choice(n_rows, size=probe, replace=False)
-    t0 = time.perf_counter()
-    ref.forward_rows(case, idx // H, idx % H, num_threads=cores)
-    dt = time.perf_counter() - t0
-    per_row = dt / probe
-    n = int(min(n_rows, max(probe, budget_s / max(per_row, 1e-9))))
-    idx = rng.choice(n_rows, size=n, replace=False)
-    t0 = time.perf_counter()
-    ref.forward_rows(case, idx // H, idx % H, num_threads=cores)
-    dt = time.perf_counter() - t0
-    full = dt * n_rows / n
-    return full, f"{n} of {n_rows} (token, head) output rows chosen uniformly (seed 0), scaled to the whole workload", cores
+    # Rows in a random order, timed in growing chunks until the budget is
+    # spent (or every row is done); the time scales by the rows processed.
+    order = rng.permutation(n_rows)
+    done, spent, chunk = 0, 0.0, max(4 * cores, 16)
+    while done < n_rows and spent < budget_s:
+        idx = order[done:done + chunk]
+        t0 = time.perf_counter()
+        ref.forward_rows(case, idx // H, idx % H, num_threads=cores)
+        spent += time.perf_counter() - t0
+        done += idx.size
+        rate = spent / done  # seconds per row
+        chunk = int(min(2 * chunk, 65536, max(cores, (budget_s - spent) / max(rate, 1e-9))))
+    full = spent * n_rows / done
+    return full, f"{done} of {n_rows} (token, head) output rows in a random order (seed 0), scaled to the whole workload", cores
 
 
 def main():
