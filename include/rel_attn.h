@@ -201,6 +201,18 @@ int32_t rel_attn_num_splits(int32_t is_local, int32_t batch_size, int32_t max_qu
                             int32_t num_heads, int32_t num_kv_heads, int32_t max_kv_len);
 
 /*
+ * rel_attn_bucket_max_seqlen_q - the query-length bucket of
+ * bucket_max_seqlen_q (vLLM API docs, fa4_rel_attention): the smallest power of
+ * two >= max_seqlen_q (1 for 0 and 1).  A caller that captures calls in a
+ * CUDA graph passes this bucket as max_seqlen_q, so one captured launch serves
+ * every batch whose longest query fits the bucket (the kernels read the actual
+ * lengths from cu_seqlens_q on the device).  Pure host integer logic.
+ * Returns the bucket, or -REL_ATTN_ERR_INVALID_ARGUMENT when max_seqlen_q < 0
+ * or the bucket would exceed 2^30.
+ */
+int32_t rel_attn_bucket_max_seqlen_q(int32_t max_seqlen_q);
+
+/*
  * rel_attn_last_error - thread-local, NUL-terminated description of the last
  * non-OK status returned on this thread ("" if none).  Owned by the library;
  * valid until the next call on the same thread.

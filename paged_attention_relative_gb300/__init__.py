@@ -9,12 +9,13 @@ from __future__ import annotations
 
 
 def __getattr__(name):
-    if name in ("rel_attn_paged_varlen", "rel_attn_num_splits", "last_launch", "set_kernel_events",
-                "device_error", "RelAttnError", "describe"):
+    if name in ("rel_attn_paged_varlen", "rel_attn_paged_varlen_noalloc", "rel_attn_num_splits",
+                "rel_attn_bucket_max_seqlen_q", "last_launch", "set_kernel_events", "device_error", "RelAttnError",
+                "describe"):
         from . import _lib
         return getattr(_lib, name)
     raise AttributeError(name)
 
 
-__all__ = ["rel_attn_paged_varlen", "rel_attn_num_splits", "last_launch", "set_kernel_events", "device_error",
-           "RelAttnError"]
+__all__ = ["rel_attn_paged_varlen", "rel_attn_paged_varlen_noalloc", "rel_attn_num_splits",
+           "rel_attn_bucket_max_seqlen_q", "last_launch", "set_kernel_events", "device_error", "RelAttnError"]

@@ -22,6 +22,7 @@ KERNELS = {0: "none", 1: "decode", 2: "prefill"}
 
 # Every function the headers declare, with its ctypes signature.
 EXPORTS = ("rel_attn_paged_varlen", "rel_attn_paged_varlen_noalloc", "rel_attn_num_splits",
+           "rel_attn_bucket_max_seqlen_q",
            "rel_attn_last_error", "rel_attn_last_launch", "rel_attn_set_kernel_events", "rel_attn_device_error")
 
 
@@ -55,6 +56,8 @@ def _load() -> ctypes.CDLL:
     lib.rel_attn_paged_varlen_noalloc.restype = ctypes.c_int
     lib.rel_attn_num_splits.argtypes = [i32] * 6
     lib.rel_attn_num_splits.restype = i32
+    lib.rel_attn_bucket_max_seqlen_q.argtypes = [i32]
+    lib.rel_attn_bucket_max_seqlen_q.restype = i32
     lib.rel_attn_last_error.argtypes = []
     lib.rel_attn_last_error.restype = ctypes.c_char_p
     lib.rel_attn_last_launch.argtypes = [ctypes.POINTER(LaunchInfo)]
@@ -143,6 +146,14 @@ def rel_attn_num_splits(is_local, batch_size, max_query_len, num_heads, num_kv_h
     """Split-KV cap (include/rel_attn.h); raises on invalid sizes."""
     r = lib.rel_attn_num_splits(int(bool(is_local)), int(batch_size), int(max_query_len), int(num_heads),
                                 int(num_kv_heads), int(max_kv_len))
+    if r < 0:
+        _check(-r)
+    return r
+
+
+def rel_attn_bucket_max_seqlen_q(max_seqlen_q) -> int:
+    """Query-length bucket for graph-captured calls (include/rel_attn.h); raises on invalid input."""
+    r = lib.rel_attn_bucket_max_seqlen_q(int(max_seqlen_q))
     if r < 0:
         _check(-r)
     return r

@@ -209,6 +209,16 @@ using namespace relattn;
 
 extern "C" const char* rel_attn_last_error(void) { return t_last_error.c_str(); }
 
+extern "C" int32_t rel_attn_bucket_max_seqlen_q(int32_t max_seqlen_q) {
+    if (max_seqlen_q < 0 || max_seqlen_q > (1 << 30)) {
+        fail(REL_ATTN_ERR_INVALID_ARGUMENT, "rel_attn_bucket_max_seqlen_q: %d outside [0, 2^30]", max_seqlen_q);
+        return -REL_ATTN_ERR_INVALID_ARGUMENT;
+    }
+    int32_t b = 1;
+    while (b < max_seqlen_q) b <<= 1;
+    return b;
+}
+
 extern "C" int32_t rel_attn_num_splits(int32_t is_local, int32_t batch_size, int32_t max_query_len,
                                        int32_t num_heads, int32_t num_kv_heads, int32_t max_kv_len) {
     if (batch_size < 1 || max_query_len < 1 || num_heads < 1 || num_kv_heads < 1 || num_heads % num_kv_heads != 0 ||

@@ -49,6 +49,15 @@ def _golden(name):
     return rows
 
 
+def test_bucket_max_seqlen_q_matches_worked_values():
+    L = _lib()
+    for n, want in _golden("bucket_max_seqlen_q.txt"):
+        assert L.rel_attn_bucket_max_seqlen_q(n) == want
+    assert L.rel_attn_bucket_max_seqlen_q(1 << 30) == 1 << 30
+    for bad in (-1, (1 << 30) + 1):
+        assert L.lib.rel_attn_bucket_max_seqlen_q(bad) == -1
+
+
 def test_num_splits_equals_oracle_on_worked_values():
     L = _lib()
     for is_local, B, mq, H, Hk, kv, cap, want in _golden("num_splits_cases.txt"):
