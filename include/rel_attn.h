@@ -134,6 +134,47 @@ rel_attn_status rel_attn_paged_varlen(
     rel_attn_stream stream);
 
 /*
+ * rel_attn_paged_varlen_lse - rel_attn_paged_varlen that also writes the
+ * log-sum-exp of each output row.  inkling_fa4_rel_attention (vLLM API docs,
+ * fa4_rel_attention) calls the attention with return_lse=False; this entry
+ * point is the return_lse=True form of the same call:
+ *
+ *   softmax_lse[t, h] = ln( sum_{allowed j} exp(s_j) ),  -inf if no key is allowed,
+ *
+ * with s_j the scaled, biased score defined above (natural logarithm, fp32).
+ * With num_splits > 1 it is the merged value of all splits.
+ *
+ * Arguments are those of rel_attn_paged_varlen plus
+ *   softmax_lse    (T, H) fp32, caller-allocated device memory, any strides >= 0
+ *                  in elements (a transposed view of an (H, T) buffer gives the
+ *                  FlashAttention layout); every (t, h) must address a distinct
+ *                  element; must not alias out or an input; 4-byte aligned.
+ *                  NULL makes the call identical to rel_attn_paged_varlen.
+ *
+ * Ownership and errors are those of rel_attn_paged_varlen, plus
+ * REL_ATTN_ERR_INVALID_ARGUMENT for a softmax_lse of the wrong dtype, rank or
+ * shape, a negative stride, misalignment, or overlap with out or an input.
+ */
+rel_attn_status rel_attn_paged_varlen_lse(
+    const rel_attn_tensor* q,
+    const rel_attn_tensor* key_cache,
+    const rel_attn_tensor* value_cache,
+    const rel_attn_tensor* block_table,
+    const rel_attn_tensor* cache_seqlens,
+    const rel_attn_tensor* cu_seqlens_q,
+    int32_t max_seqlen_q,
+    float softmax_scale,
+    int32_t causal,
+    int32_t window_left,
+    int32_t window_right,
+    int32_t rel_extent,
+    const rel_attn_tensor* rel_logits,
+    int32_t num_splits,
+    rel_attn_tensor* out,
+    rel_attn_tensor* softmax_lse,
+    rel_attn_stream stream);
+
+/*
  * rel_attn_paged_varlen_noalloc - the same forward for the decode path
  * (max_seqlen_q * num_heads / num_kv_heads <= 64) that allocates no device
  * memory.  It has no counterpart on the pages that define the attention; it

@@ -112,12 +112,14 @@ def forward_rows(c, rows_t, rows_h, num_threads: int | None = None) -> np.ndarra
     return out
 
 
-def brute_force(c) -> np.ndarray:
+def brute_force(c, with_lse: bool = False):
     """Pure-Python loops over every (token, head, key, dim); tiny inputs only.
 
     Written independently of the C file: per output row it walks the request's
     keys, builds the score list with the bias rule of score_mod_rel_bias
     (distance, zero outside [0, R)), and takes the softmax-weighted mean of V.
+    With ``with_lse`` it also returns log(sum exp(score)) per (token, head),
+    -inf where no key is visible.
     """
     q = c.q.double().tolist()
     kc = c.key_cache.double().tolist()
@@ -133,6 +135,7 @@ def brute_force(c) -> np.ndarray:
     scale = float(np.float32(c.softmax_scale))
     wl, wr = c.window_left, c.window_right
     out = [[[0.0] * D for _ in range(H)] for _ in range(T)]
+    lse = [[-math.inf] * H for _ in range(T)]
     for b in range(len(seqk)):
         n_q = cu[b + 1] - cu[b]
         n_k = seqk[b]
@@ -162,7 +165,9 @@ def brute_force(c) -> np.ndarray:
                 w = [math.exp(s - top) for s in scores]
                 tot = sum(w)
                 out[t][h] = [sum(w[n] * values[n][e] for n in range(len(w))) / tot for e in range(D)]
-    return np.array(out, dtype=np.float64).reshape(T, H, D)
+                lse[t][h] = top + math.log(tot)
+    o = np.array(out, dtype=np.float64).reshape(T, H, D)
+    return (o, np.array(lse, dtype=np.float64).reshape(T, H)) if with_lse else o
 
 
 # ---------------------------------------------------------------------------

@@ -21,7 +21,7 @@ STATUS = {0: "OK", 1: "INVALID_ARGUMENT", 2: "UNSUPPORTED", 3: "CUDA", 4: "OUT_O
 KERNELS = {0: "none", 1: "decode", 2: "prefill"}
 
 # Every function the headers declare, with its ctypes signature.
-EXPORTS = ("rel_attn_paged_varlen", "rel_attn_paged_varlen_noalloc", "rel_attn_num_splits",
+EXPORTS = ("rel_attn_paged_varlen", "rel_attn_paged_varlen_lse", "rel_attn_paged_varlen_noalloc", "rel_attn_num_splits",
            "rel_attn_bucket_max_seqlen_q",
            "rel_attn_last_error", "rel_attn_last_launch", "rel_attn_set_kernel_events", "rel_attn_device_error")
 
@@ -52,6 +52,9 @@ def _load() -> ctypes.CDLL:
     i32, f32 = ctypes.c_int32, ctypes.c_float
     lib.rel_attn_paged_varlen.argtypes = [P, P, P, P, P, P, i32, f32, i32, i32, i32, i32, P, i32, P, ctypes.c_void_p]
     lib.rel_attn_paged_varlen.restype = ctypes.c_int
+    lib.rel_attn_paged_varlen_lse.argtypes = [P, P, P, P, P, P, i32, f32, i32, i32, i32, i32, P, i32, P, P,
+                                              ctypes.c_void_p]
+    lib.rel_attn_paged_varlen_lse.restype = ctypes.c_int
     lib.rel_attn_paged_varlen_noalloc.argtypes = lib.rel_attn_paged_varlen.argtypes
     lib.rel_attn_paged_varlen_noalloc.restype = ctypes.c_int
     lib.rel_attn_num_splits.argtypes = [i32] * 6
@@ -121,6 +124,34 @@ def rel_attn_paged_varlen(q, key_cache, value_cache, block_table, cache_seqlens,
                                    _ref(rel), int(num_splits), _ref(od), ctypes.c_void_p(stream))
     _check(st)
     return out
+
+
+def rel_attn_paged_varlen_lse(q, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_q, max_seqlen_q,
+                              softmax_scale, causal, window_left, window_right, rel_extent, rel_logits, num_splits,
+                              out=None, softmax_lse=None, stream=None):
+    """The forward that also writes each row's natural-log sum-exp; see include/rel_attn.h.
+
+    Returns ``(out, softmax_lse)``.  ``softmax_lse`` is allocated as a
+    contiguous ``(T, H)`` fp32 tensor when None; any ``(T, H)`` fp32 view
+    works (``lse_ht.t()`` for an ``(H, T)`` buffer).
+    """
+    if out is None:
+        out = torch.empty_like(q)
+    if softmax_lse is None:
+        softmax_lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    descs = [describe(t) for t in (q, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_q)]
+    rel = describe(rel_logits) if rel_extent > 0 else None
+    od = describe(out)
+    ld = describe(softmax_lse)
+    st = lib.rel_attn_paged_varlen_lse(*[_ref(d) for d in descs], int(max_seqlen_q), float(softmax_scale),
+                                       int(bool(causal)), int(window_left), int(window_right), int(rel_extent),
+                                       _ref(rel), int(num_splits), _ref(od), _ref(ld), ctypes.c_void_p(stream))
+    _check(st)
+    return out, softmax_lse
 
 
 def rel_attn_paged_varlen_noalloc(q, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_q,

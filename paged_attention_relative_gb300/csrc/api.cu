@@ -280,12 +280,15 @@ extern "C" rel_attn_status rel_attn_device_error(int32_t* code) {
     return REL_ATTN_OK;
 }
 
-extern "C" rel_attn_status rel_attn_paged_varlen(
+namespace {
+
+// Body of rel_attn_paged_varlen and rel_attn_paged_varlen_lse (lse may be NULL).
+rel_attn_status paged_varlen(
     const rel_attn_tensor* q, const rel_attn_tensor* key_cache, const rel_attn_tensor* value_cache,
     const rel_attn_tensor* block_table, const rel_attn_tensor* cache_seqlens, const rel_attn_tensor* cu_seqlens_q,
     int32_t max_seqlen_q, float softmax_scale, int32_t causal, int32_t window_left, int32_t window_right,
     int32_t rel_extent, const rel_attn_tensor* rel_logits, int32_t num_splits, rel_attn_tensor* out,
-    rel_attn_stream stream_) {
+    rel_attn_tensor* lse, rel_attn_stream stream_) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     t_launch = rel_attn_launch_info{};
     rel_attn_status st;
@@ -346,6 +349,19 @@ extern "C" rel_attn_status rel_attn_paged_varlen(
     if (overlaps(out, out_elem, q, 2) || overlaps(out, out_elem, key_cache, 2) ||
         overlaps(out, out_elem, value_cache, 2) || (rel_extent > 0 && overlaps(out, out_elem, rel_logits, 2)))
         return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "out aliases an input");
+    if (lse) {
+        if ((st = check_tensor(lse, "softmax_lse", REL_ATTN_F32, 2))) return st;
+        if (lse->shape[0] != T || lse->shape[1] != H)
+            return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "softmax_lse must be (T, H)");
+        if (lse->stride[0] < 0 || lse->stride[1] < 0)
+            return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "softmax_lse strides must be >= 0");
+        if (overlaps(lse, 4, q, 2) || overlaps(lse, 4, key_cache, 2) || overlaps(lse, 4, value_cache, 2) ||
+            overlaps(lse, 4, block_table, 4) || overlaps(lse, 4, cache_seqlens, 4) ||
+            overlaps(lse, 4, cu_seqlens_q, 4) || overlaps(lse, 4, out, out_elem) ||
+            (rel_extent > 0 && overlaps(lse, 4, rel_logits, 2)))
+            return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "softmax_lse aliases an input or out");
+        if (!aligned(lse->data, 4)) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "softmax_lse is not 4-byte aligned");
+    }
     if (T == 0 || B == 0) {
         t_launch.kernel = REL_ATTN_KERNEL_NONE;
         return REL_ATTN_OK;
@@ -410,6 +426,11 @@ extern "C" rel_attn_status rel_attn_paged_varlen(
     p.o_st = out->stride[0];
     p.o_sh = out->stride[1];
     p.out_f32 = out->dtype == REL_ATTN_F32 ? 1 : 0;
+    if (lse) {
+        p.lse = static_cast<float*>(lse->data);
+        p.lse_st = lse->stride[0];
+        p.lse_sh = lse->stride[1];
+    }
     p.B = (int32_t)B;
     p.T = (int32_t)T;
     p.H = (int32_t)H;
@@ -490,6 +511,30 @@ extern "C" rel_attn_status rel_attn_paged_varlen(
     t_launch.workspace_bytes = (int64_t)ws_bytes;
     if (e != cudaSuccess) return fail(REL_ATTN_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
     return REL_ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" rel_attn_status rel_attn_paged_varlen(
+    const rel_attn_tensor* q, const rel_attn_tensor* key_cache, const rel_attn_tensor* value_cache,
+    const rel_attn_tensor* block_table, const rel_attn_tensor* cache_seqlens, const rel_attn_tensor* cu_seqlens_q,
+    int32_t max_seqlen_q, float softmax_scale, int32_t causal, int32_t window_left, int32_t window_right,
+    int32_t rel_extent, const rel_attn_tensor* rel_logits, int32_t num_splits, rel_attn_tensor* out,
+    rel_attn_stream stream) {
+    return paged_varlen(q, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_q, max_seqlen_q,
+                        softmax_scale, causal, window_left, window_right, rel_extent, rel_logits, num_splits, out,
+                        nullptr, stream);
+}
+
+extern "C" rel_attn_status rel_attn_paged_varlen_lse(
+    const rel_attn_tensor* q, const rel_attn_tensor* key_cache, const rel_attn_tensor* value_cache,
+    const rel_attn_tensor* block_table, const rel_attn_tensor* cache_seqlens, const rel_attn_tensor* cu_seqlens_q,
+    int32_t max_seqlen_q, float softmax_scale, int32_t causal, int32_t window_left, int32_t window_right,
+    int32_t rel_extent, const rel_attn_tensor* rel_logits, int32_t num_splits, rel_attn_tensor* out,
+    rel_attn_tensor* softmax_lse, rel_attn_stream stream) {
+    return paged_varlen(q, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_q, max_seqlen_q,
+                        softmax_scale, causal, window_left, window_right, rel_extent, rel_logits, num_splits, out,
+                        softmax_lse, stream);
 }
 
 namespace relattn {

@@ -1,6 +1,7 @@
 // Split-KV combine: out[t,h,:] = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M),
 // M = max_s lse_s, where o_s is split s's normalised partial output and lse_s
 // its log2-sum-exp; a row whose every split is empty (all lse = -inf) gets 0.
+// When requested, the row's natural-log sum-exp (M + log2 sum) * ln 2 goes to lse.
 // One warp per (token, head) row, D/32 contiguous dims per lane.
 //
 // The split count is the num_splits argument of inkling_fa4_rel_attention
@@ -38,6 +39,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const AttnParams p) {
     float acc[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) acc[i] = 0.f;
+    float lse_row = -CUDART_INF_F;  // natural log of the merged sum-exp
     if (mx != -CUDART_INF_F) {
         float L = 0.f;
         const float* base = p.ws_o + (size_t)row * D + lane * V;
@@ -79,8 +81,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const AttnParams p) {
         const float inv = 1.f / L;
 #pragma unroll
         for (int i = 0; i < V; ++i) acc[i] *= inv;
+        lse_row = (mx + __log2f(L)) * kLn2;
     }
     const int t = (int)(row / p.H), h = (int)(row % p.H);
+    if (p.lse && lane == 0) p.lse[(size_t)t * p.lse_st + (size_t)h * p.lse_sh] = lse_row;
     const size_t oo = (size_t)t * p.o_st + (size_t)h * p.o_sh + lane * V;
     if (p.out_f32) {
         float* dst = reinterpret_cast<float*>(p.out) + oo;

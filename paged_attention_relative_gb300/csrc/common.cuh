@@ -9,6 +9,8 @@
 
 namespace relattn {
 
+constexpr float kLn2 = 0.6931471805599453f;  // converts base-2 log-sum-exp to natural units
+
 enum WaitSite : int {
     kSiteDecodeFull = 1,
     kSiteDecodeEmpty = 2,

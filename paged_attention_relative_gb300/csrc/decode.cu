@@ -425,6 +425,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, KSL>::kMaxThreads) decode_ker
                 pk.y = pack_bf16(acc.z, acc.w);
                 *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.out) + oo) = pk;
             }
+            // natural-log sum-exp: M and log2 L are in base-2 units
+            if (p.lse && c4 == 0)
+                p.lse[(size_t)t * p.lse_st + (size_t)h * p.lse_sh] =
+                    M == -CUDART_INF_F ? -CUDART_INF_F : (M + __log2f(L)) * kLn2;
         } else {
             const size_t row = ((size_t)split * p.T + t) * p.H + h;
             *reinterpret_cast<float4*>(p.ws_o + row * D + c4 * 4) = acc;

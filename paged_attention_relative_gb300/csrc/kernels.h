@@ -25,6 +25,8 @@ struct AttnParams {
     void* out;                 // (T, H, D) bf16, or fp32 when out_f32
     int64_t o_st, o_sh;
     int32_t out_f32;
+    float* lse;                // (T, H) fp32 natural-log sum-exp of each row's scores, or null
+    int64_t lse_st, lse_sh;    // token / head strides of lse
     float* ws_o;               // (S, T, H, D) fp32 partials when num_splits > 1
     float* ws_lse;             // (S, T, H) fp32 log2-sum-exp partials
     int32_t B, T, H, Hk, G, BS, D;
@@ -66,7 +68,7 @@ int prefill_bias_window();
 cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap* maps, const LaunchShape& shape,
                            cudaStream_t stream);
 
-// LSE-weighted merge of split partials into bf16 out.
+// LSE-weighted merge of split partials into out (and lse when requested).
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t stream);
 
 }  // namespace relattn

@@ -746,6 +746,8 @@ __global__ void __launch_bounds__(384, 1)
         if (valid && partial && half == 0)
             p.ws_lse[((size_t)split * p.T + t) * p.H + h] =
                 l_tot > 0.f ? m_run * kLog2e + __log2f(l_tot) : -CUDART_INF_F;
+        if (valid && !partial && half == 0 && p.lse)
+            p.lse[(size_t)t * p.lse_st + (size_t)h * p.lse_sh] = l_tot > 0.f ? m_run + logf(l_tot) : -CUDART_INF_F;
     }
 
     tc_fence_before();

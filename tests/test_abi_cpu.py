@@ -167,3 +167,20 @@ def test_empty_batch_is_a_no_op():
                 cu_seqlens_q=torch.zeros(3, dtype=torch.int32), max_seqlen_q=0)
     assert out.shape[0] == 0
     assert L.last_launch()["kernel"] == "none"
+
+
+@pytest.mark.parametrize("make_lse", [
+    lambda c, out: torch.empty(c.q.shape[0], c.q.shape[1] + 1, dtype=torch.float32),   # wrong shape
+    lambda c, out: torch.empty(c.q.shape[0], c.q.shape[1], dtype=torch.bfloat16),      # wrong dtype
+    lambda c, out: torch.empty(c.q.shape[0], dtype=torch.float32),                     # wrong rank
+    lambda c, out: out.view(torch.float32)[:, :, 0],                                   # aliases out
+], ids=["shape", "dtype", "rank", "aliases_out"])
+def test_lse_argument_is_validated_before_device_work(make_lse):
+    L = _lib()
+    c = _cpu_case()
+    out = torch.empty_like(c.q)
+    with pytest.raises(L.RelAttnError) as ei:
+        L.rel_attn_paged_varlen_lse(c.q, c.key_cache, c.value_cache, c.block_table, c.cache_seqlens,
+                                    c.cu_seqlens_q, c.max_seqlen_q, c.softmax_scale, c.causal, -1, -1,
+                                    c.rel_extent, c.rel_logits, 1, out=out, softmax_lse=make_lse(c, out), stream=0)
+    assert ei.value.status == 1

@@ -58,6 +58,16 @@ def test_c_oracle_equals_python_brute_force(i):
     np.testing.assert_allclose(ref.forward(c), ref.brute_force(c), rtol=0, atol=1e-12)
 
 
+@pytest.mark.parametrize("i", range(len(BRUTE_CASES)))
+def test_c_oracle_lse_equals_python_brute_force(i):
+    c = _small(100 + i, **BRUTE_CASES[i])
+    _, lse = ref.forward(c, with_lse=True)
+    _, want = ref.brute_force(c, with_lse=True)
+    assert np.array_equal(np.isneginf(lse), np.isneginf(want))
+    fin = np.isfinite(want)
+    np.testing.assert_allclose(lse[fin], want[fin], rtol=0, atol=1e-12)
+
+
 def test_tiny_mixed_c_oracle_equals_brute_force():
     c = tiny_mixed(0)
     np.testing.assert_allclose(ref.forward(c), ref.brute_force(c), rtol=0, atol=1e-12)
@@ -121,14 +131,32 @@ def test_zero_query_zero_bias_is_mean_of_allowed_values(window):
             np.testing.assert_allclose(got[i, h], want[h // 2].numpy(), rtol=0, atol=1e-12)
 
 
+@pytest.mark.parametrize("window", [(-1, -1), (3, 0), (0, 0)])
+def test_zero_scores_give_lse_log_of_visible_key_count(window):
+    """Every visible score is 0, so lse = ln(number of visible keys)."""
+    c = _small(10, seqlens_q=[4], seqlens_k=[11], window=window, rel_extent=4)
+    c = c.with_(q=torch.zeros_like(c.q), rel_logits=torch.zeros_like(c.rel_logits))
+    _, lse = ref.forward(c, with_lse=True)
+    for i in range(4):
+        pos = i + 7
+        lo = 0 if window[0] < 0 else max(0, pos - window[0])
+        np.testing.assert_allclose(lse[i], math.log(pos + 1 - lo), rtol=0, atol=1e-12)
+
+
 def test_rows_without_keys_are_zero():
     """sk < sq, bottom-right causal: rows 0..2 of a 5-row request over 2 keys
     see no key; rows 3 and 4 see keys {0} and {0,1}."""
     c = _small(11, seqlens_q=[5], seqlens_k=[2])
     c = c.with_(q=torch.zeros_like(c.q))
-    got = ref.forward(c)
+    got, lse = ref.forward(c, with_lse=True)
     v = _kv_contig(c, 0, "v")
     assert np.all(got[:3] == 0.0)
+    assert np.all(np.isneginf(lse[:3]))
+    for h in range(4):
+        # q = 0: row 3 sees key 0 at distance 0, row 4 keys 0 and 1 at distances 1 and 0
+        assert lse[3, h] == float(c.rel_logits[3, h, 0])
+        b1, b0 = float(c.rel_logits[4, h, 1]), float(c.rel_logits[4, h, 0])
+        assert abs(lse[4, h] - math.log(math.exp(b1) + math.exp(b0))) < 1e-12
     for h in range(4):
         assert np.array_equal(got[3, h], v[0, h // 2].numpy())
         # two keys with scores b(d=1), b(d=0) from the bias alone
@@ -221,7 +249,11 @@ def test_bias_shift_invariance_when_every_key_is_in_band():
     base = torch.round(c.rel_logits.float().clamp(-8, 8) * 4) / 4
     c = c.with_(rel_logits=base.to(torch.bfloat16))
     c2 = c.with_(rel_logits=(base + 3.0).to(torch.bfloat16))
-    np.testing.assert_allclose(ref.forward(c), ref.forward(c2), rtol=0, atol=1e-12)
+    o1, l1 = ref.forward(c, with_lse=True)
+    o2, l2 = ref.forward(c2, with_lse=True)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-12)
+    # the shift moves every visible score, so the log-sum-exp moves by exactly 3
+    np.testing.assert_allclose(l2, l1 + 3.0, rtol=0, atol=1e-12)
 
 
 def test_rows_entry_equals_full_forward():
