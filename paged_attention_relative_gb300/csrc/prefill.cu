@@ -15,15 +15,20 @@
 //              arrives as 2 KB TMA boxes (16 keys x 64 dims) straight from the
 //              paged cache, one per fully visible 16-key group, multicast to
 //              the other CTA of the cluster (the two take turns issuing), with
-//              block-table entries fetched two tiles ahead; groups only
-//              partly inside the visible range go through zero-filling
-//              cp.async (proxy-fenced once landed).  Tiles are 128-byte
-//              swizzled; a slot's full mbarrier takes the TMA bytes plus one
-//              arrival per producer lane, its empty mbarrier one MMA commit
-//              per CTA of the cluster.
+//              block-table entries fetched a 4-tile window ahead (one
+//              coalesced load per window); groups only partly inside the
+//              visible range go through zero-filling cp.async (proxy-fenced
+//              once landed).  Tiles are 128-byte swizzled; a slot's full
+//              mbarrier takes the TMA bytes plus the producer's arrivals, its
+//              empty mbarrier one MMA commit per CTA of the cluster.  Each
+//              producer's per-tile work is on the critical path (a TMA issue
+//              costs ~90 cycles per box even spread over lanes), so the loop
+//              keeps nothing else in it: no global loads, no divisions.
 //   warp 1     bias windows: for each band tile (one that reaches some row's
-//              bias band) it stages that tile's rel_logits by TMA once the
-//              softmax warps have read the previous band tile's (see below).
+//              bias band) it stages that tile's rel_logits by TMA into one of
+//              two window buffers (one with D = 64) once the softmax warps
+//              have released that buffer's previous fill (see below), so the
+//              next band tile's windows load while the current one is read.
 //   warp 3     MMA issuer (one thread) and TMEM owner: S_j = Q K_j^T into one
 //              of two TMEM buffers (M=128, N=128, K=head_dim, Q read from
 //              TMEM), then O += P_{j-1} V_{j-1} with P read from TMEM and V
@@ -83,7 +88,7 @@ struct PrefillCfg {
     static constexpr int kMmaWarp = 3;
     static constexpr int kSoftThreads = 256;        // warps 4-11
     static constexpr int kThreads = 384;
-    static constexpr int kKRing = D == 128 ? 3 : 6;   // K tile slots
+    static constexpr int kKRing = D == 128 ? 2 : 6;   // K tile slots
     static constexpr int kVRing = D == 128 ? 2 : 4;   // V tile slots (after the K ring)
     static constexpr int kStages = kKRing + kVRing;
     // rel_logits values per staged bias row: at least 128 + 14 (a tile plus the
@@ -92,8 +97,10 @@ struct PrefillCfg {
     static constexpr int kBiasW = 152;
     // 128 rows, plus up to 16 token sub-boxes each padded to a 128-byte boundary
     static constexpr int kBiasBytes = 128 * kBiasW * 2 + 16 * 128;
+    // Band tiles' windows are double-buffered where shared memory allows.
+    static constexpr int kBiasBufs = D == 128 ? 2 : 1;
     static constexpr int kXchBytes = 3 * 2 * 128 * 4;  // half-row maxima (2 tile buffers), half-row sums
-    static constexpr int kData = kStages * kTileBytes + kBiasBytes + kXchBytes;
+    static constexpr int kData = kStages * kTileBytes + kBiasBufs * kBiasBytes + kXchBytes;
     static constexpr int kTmemCols = 512;
     static constexpr int kOCol = 256;      // O: D columns
     static constexpr int kQCol = 256 + D;  // Q: D / 2 columns (bf16 pairs)
@@ -108,8 +115,8 @@ struct PrefillBars {
     uint64_t x_full[2];      // per tile parity: every softmax warp has published its half-row maxima
     uint64_t o_done;   // one phase per PV tile (rescale waits, never more than one phase behind)
     uint64_t o_final;  // single phase: every MMA of the CTA has completed
-    uint64_t bias_full;   // one phase per band tile: its rel_logits windows have landed
-    uint64_t bias_empty;  // one phase per band tile: every softmax warp has read its windows
+    uint64_t bias_full[2];   // per window buffer, one phase per fill: its rel_logits windows have landed
+    uint64_t bias_empty[2];  // per window buffer, one phase per fill: every softmax warp has read them
     uint32_t tmem_base;
     int abort;
 };
@@ -131,8 +138,8 @@ __global__ void __launch_bounds__(384, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sKV = smem;
     uint8_t* sBias = sKV + C::kStages * C::kTileBytes;
-    float* sXch = reinterpret_cast<float*>(sBias + C::kBiasBytes);  // [3 bufs][2 halves][128 rows]
-    PrefillBars* bars = reinterpret_cast<PrefillBars*>(sBias + C::kBiasBytes + C::kXchBytes);
+    float* sXch = reinterpret_cast<float*>(sBias + C::kBiasBufs * C::kBiasBytes);  // [3 bufs][2 halves][128 rows]
+    PrefillBars* bars = reinterpret_cast<PrefillBars*>(sBias + C::kBiasBufs * C::kBiasBytes + C::kXchBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.G, TPT = 128 / G;
@@ -209,8 +216,10 @@ __global__ void __launch_bounds__(384, 1)
         }
         mbar_init(&bars->o_done, 1);
         mbar_init(&bars->o_final, 1);
-        mbar_init(&bars->bias_full, 1);
-        mbar_init(&bars->bias_empty, C::kSoftThreads / 32);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->bias_full[i], 1);
+            mbar_init(&bars->bias_empty[i], C::kSoftThreads / 32);
+        }
         bars->abort = 0;
         fence_mbar_init();
     }
@@ -272,37 +281,44 @@ __global__ void __launch_bounds__(384, 1)
             mbar_arrive(pend);
             pend = nullptr;
         };
-        // Block-table entries run two tiles ahead of the copies: lane l < 8
-        // holds the physical block of 16-key group l of a tile.
-        auto load_bt = [&](int jj) -> int {
+        // Block-table windows of 4 tiles: lane l holds the physical block of
+        // 16-key group l % 8 of tile w0 + l / 8; the next window is fetched
+        // one window ahead (32 consecutive entries when BS is 16).
+        auto load_win = [&](int w0) -> int {
             int v = 0;
-            if (lane < 8 && jj < n_it) {
-                const int jg = key_block(jj) * C::BN + 16 * lane;
+            const int jw = w0 + (lane >> 3);
+            if (jw < n_it) {
+                const int jg = key_block(jw) * C::BN + 16 * (lane & 7);
                 if (jg + 15 >= lo && jg < hi) v = __ldg(bt + jg / p.BS);
             }
             return v;
         };
-        int bt_cur = load_bt(0), bt_n1 = load_bt(1), bt_n2 = load_bt(2);
+        int win_cur = load_win(0), win_nxt = load_win(4);
         // TMA lanes: lane -> (16-key group lane / kDB, 64-dim block lane % kDB).
         const int t_pg = lane / C::kDB, t_db = lane % C::kDB;
         const int ring0 = is_v ? C::kKRing : 0;
         const int ring = is_v ? C::kVRing : C::kKRing;
+        int sidx = 0;
+        uint32_t eph = 1;  // parity of the empty phase to wait for
         for (int jj = 0; jj < n_it; ++jj) {
-            const int slot = ring0 + jj % ring;
-            const int round = jj / ring;
+            const int slot = ring0 + sidx;
             // Never block on a full ring while holding copies whose landing has
             // not been signalled: the consumer may be waiting for exactly those.
-            if (!mbar_try_wait(&bars->kv_empty[slot], (round & 1) ^ 1)) {
+            if (!mbar_try_wait(&bars->kv_empty[slot], eph)) {
                 if (pend) retire(0);
-                if (!mbar_wait(&bars->kv_empty[slot], (round & 1) ^ 1, p.timeout_ns, kSitePrefillKEmpty, p.err))
+                if (!mbar_wait(&bars->kv_empty[slot], eph, p.timeout_ns, kSitePrefillKEmpty, p.err))
                     bars->abort = 1;
             }
-            if (__any_sync(0xffffffffu, aborted(bars))) break;
-            if (jj >= 1) {
-                bt_cur = bt_n1;
-                bt_n1 = bt_n2;
-                bt_n2 = load_bt(jj + 2);
+            if (++sidx == ring) {
+                sidx = 0;
+                eph ^= 1;
             }
+            if (__any_sync(0xffffffffu, aborted(bars))) break;
+            if (jj >= 4 && (jj & 3) == 0) {
+                win_cur = win_nxt;
+                win_nxt = load_win(jj + 4);
+            }
+            const int wl = (jj & 3) * 8;
             const int j0 = key_block(jj) * C::BN;
             // Bit pg set: 16-key group pg is fully visible (whole-box TMA).
             uint32_t full_mask = 0;
@@ -315,7 +331,7 @@ __global__ void __launch_bounds__(384, 1)
             uint8_t* tile = sKV + slot * C::kTileBytes;
             if (lane == 0) mbar_arrive_expect_tx(full_bar, (uint32_t)__popc(full_mask) * C::kDB * 2048u);
             __syncwarp();
-            const int blk_t = min(max(__shfl_sync(0xffffffffu, bt_cur, t_pg & 7), 0), p.NB - 1);
+            const int blk_t = min(max(__shfl_sync(0xffffffffu, win_cur, wl + (t_pg & 7)), 0), p.NB - 1);
             if (lane < 8 * C::kDB && ((full_mask >> t_pg) & 1) && lane % n_act == my_idx) {
                 const int jg = j0 + 16 * t_pg;
                 tma_load_4d_mc(tile + t_db * C::kBlk + t_pg * 16 * 128, tmap, full_bar, 64 * t_db, g, jg % p.BS,
@@ -327,7 +343,7 @@ __global__ void __launch_bounds__(384, 1)
                 for (int pg = 0; pg < 8; ++pg) {
                     if ((full_mask >> pg) & 1) continue;
                     const int jg = j0 + 16 * pg;
-                    const int blk = min(max(__shfl_sync(0xffffffffu, bt_cur, pg), 0), p.NB - 1);
+                    const int blk = min(max(__shfl_sync(0xffffffffu, win_cur, wl + pg), 0), p.NB - 1);
                     const uint16_t* src = cache + (long long)blk * p.c_s0 + (long long)(jg % p.BS) * p.c_s1 +
                                           (long long)g * p.c_s2 + lane_off;
 #pragma unroll
@@ -343,10 +359,12 @@ __global__ void __launch_bounds__(384, 1)
                 cp_async_commit();
             }
             if (pend) retire(part ? 1 : 0);
-            if (part)
+            if (part) {
                 pend = full_bar;
-            else
-                mbar_arrive(full_bar);
+            } else {
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cnt(full_bar, 32);
+            }
         }
         if (pend) retire(0);
         // Wait until every active CTA has released each slot for the last
@@ -373,19 +391,21 @@ __global__ void __launch_bounds__(384, 1)
             for (int jj = 0; jj < n_it; ++jj) {
                 const int j0 = key_block(jj) * C::BN;
                 if (!band_tile(j0)) continue;
-                if (nbi > 0 && !mbar_wait(&bars->bias_empty, (nbi - 1) & 1, p.timeout_ns, kSitePrefillRelEmpty,
+                // Buffer bb's fill number `use` waits for the softmax to release fill use - 1.
+                const int bb = nbi % C::kBiasBufs, use = nbi / C::kBiasBufs;
+                if (use > 0 && !mbar_wait(&bars->bias_empty[bb], (use - 1) & 1, p.timeout_ns, kSitePrefillRelEmpty,
                                           p.err)) {
                     bars->abort = 1;
                     break;
                 }
                 if (aborted(bars)) break;
                 fence_proxy_async_smem();
-                mbar_arrive_expect_tx(&bars->bias_full, (uint32_t)(n_sub * TS * G * C::kBiasW * 2));
+                mbar_arrive_expect_tx(&bars->bias_full[bb], (uint32_t)(n_sub * TS * G * C::kBiasW * 2));
                 for (int sbx = 0; sbx < n_sub; ++sbx) {
                     const int ts = i0 + sbx * TS;
                     const int a = ts + off - j0 - 127;
-                    tma_load_3d_hint(sBias + sbx * sub_bytes, &tm_rel, &bars->bias_full, a - (a & 7), g * G,
-                                     q0 + ts, pol);
+                    tma_load_3d_hint(sBias + bb * C::kBiasBytes + sbx * sub_bytes, &tm_rel, &bars->bias_full[bb],
+                                     a - (a & 7), g * G, q0 + ts, pol);
                 }
                 ++nbi;
             }
@@ -557,11 +577,14 @@ __global__ void __launch_bounds__(384, 1)
                     const float2 sc2 = make_float2(sc, sc);
                     if (band) {
                         if constexpr (VEC) {
-                            if (!mbar_wait(&bars->bias_full, nb & 1, p.timeout_ns, kSitePrefillRelFull, p.err))
+                            const int bb = nb % C::kBiasBufs;
+                            if (!mbar_wait(&bars->bias_full[bb], (nb / C::kBiasBufs) & 1, p.timeout_ns,
+                                           kSitePrefillRelFull, p.err))
                                 bars->abort = 1;
+                            const uint32_t* wb = wrow + bb * (C::kBiasBytes / 4);
                             uint32_t wv[33];
 #pragma unroll
-                            for (int i = 0; i < 33; ++i) wv[i] = wrow[i];
+                            for (int i = 0; i < 33; ++i) wv[i] = wb[i];
 #pragma unroll
                             for (int e = 0; e < 32; ++e) {
                                 const uint32_t pr = __byte_perm(wv[31 - e], wv[32 - e], psel);
@@ -570,7 +593,7 @@ __global__ void __launch_bounds__(384, 1)
                             }
                             // Every read of this band tile's windows is done.
                             __syncwarp();
-                            if (lane == 0) mbar_arrive(&bars->bias_empty);
+                            if (lane == 0) mbar_arrive(&bars->bias_empty[bb]);
                         } else {
 #pragma unroll
                             for (int e = 0; e < 32; ++e) {
