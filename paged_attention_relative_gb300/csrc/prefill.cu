@@ -127,6 +127,44 @@ __device__ __forceinline__ bool aborted(const PrefillBars* bars) {
 
 __device__ __forceinline__ int floor_div8(int x) { return x >= 0 ? x >> 3 : -((-x + 7) >> 3); }
 
+// Batches up to this size launch one cluster per (request, pair of query
+// tiles) that has rows, found by a scan over cu_seqlens_q; larger ones launch
+// max_seqlen_q's tile count for every request and let empty clusters leave.
+constexpr int kCompactMaxB = 256;
+
+// Cluster ci of a compact launch -> (request, top query tile of its pair), or
+// request -1 past the last pair.  Requests in order; within a request the
+// pairs go from the last (most keys) to the first.  Warp-collective: every
+// lane gets the same answer.
+__device__ __forceinline__ int2 compact_cluster_tile(const int32_t* cu, int B, int TPT, int ci) {
+    const int lane = threadIdx.x & 31;
+    int base = 0;
+    for (int b0 = 0; b0 < B; b0 += 32) {
+        const int bb = b0 + lane;
+        int n = 0;
+        if (bb < B) {
+            const int nt = (__ldg(cu + bb + 1) - __ldg(cu + bb) + TPT - 1) / TPT;
+            n = (nt + kCluster - 1) / kCluster;
+        }
+        int inc = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += v;
+        }
+        const int tot = __shfl_sync(0xffffffffu, inc, 31);
+        if (ci < base + tot) {
+            const int src = __ffs(__ballot_sync(0xffffffffu, base + inc > ci)) - 1;
+            const int first = base + __shfl_sync(0xffffffffu, inc - n, src);
+            const int nb = __shfl_sync(0xffffffffu, n, src);
+            const int k = nb - 1 - (ci - first);
+            return make_int2(b0 + src, k * kCluster + kCluster - 1);
+        }
+        base += tot;
+    }
+    return make_int2(-1, 0);
+}
+
 // VEC: rel_logits rows are 16-byte aligned (R % 8 == 0), so bias windows are
 // staged by 16-byte copies; otherwise the bias is read per element.
 template <int D, bool VEC>
@@ -143,10 +181,21 @@ __global__ void __launch_bounds__(384, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.G, TPT = 128 / G;
-    const int qt = gridDim.x - 1 - blockIdx.x;  // longest tiles first
+    const int crank = (int)cluster_ctarank();
     const int g = blockIdx.y;
     const int S = p.num_splits;
-    const int b = blockIdx.z / S, split = blockIdx.z % S;
+    int qt, b, split;
+    if (p.B <= kCompactMaxB) {
+        const int2 ct = compact_cluster_tile(p.cu_seqlens_q, p.B, TPT, (int)(blockIdx.x / kCluster));
+        if (ct.x < 0) return;  // past the last pair (the same in every CTA of the cluster)
+        b = ct.x;
+        qt = ct.y - crank;
+        split = blockIdx.z;
+    } else {
+        qt = gridDim.x - 1 - blockIdx.x;  // longest tiles first
+        b = blockIdx.z / S;
+        split = blockIdx.z % S;
+    }
     const int q0 = p.cu_seqlens_q[b];
     const int sq = p.cu_seqlens_q[b + 1] - q0;
     const int sk = p.cache_seqlens[b];
@@ -161,7 +210,6 @@ __global__ void __launch_bounds__(384, 1)
     // kv head, split) and walk one shared sequence of K/V tiles: the union of
     // their visible ranges.  Rank r holds tile qt_top - r; CTAs whose tile is
     // past the request's end are inactive (no loads, no MMAs).
-    const int crank = (int)cluster_ctarank();
     const int qt_top = qt + crank;
     uint32_t active = 0;
 #pragma unroll
@@ -817,7 +865,16 @@ LaunchShape prefill_shape(const AttnParams& p) {
     LaunchShape s;
     const int tpt = 128 / p.G;
     const int qtiles = (p.max_seqlen_q + tpt - 1) / tpt;
-    s.grid = dim3((qtiles + kCluster - 1) / kCluster * kCluster, p.Hk, p.B * p.num_splits);
+    if (p.B <= kCompactMaxB) {
+        // Pairs with rows: at most ceil(qtiles / 2) per request, and at most
+        // one partly filled pair per request beyond T / (2 * tpt) full ones.
+        const long long per_req = (qtiles + kCluster - 1) / kCluster;
+        const long long by_rows = ((long long)p.T + kCluster * tpt - 1) / (kCluster * tpt) + p.B;
+        const long long n_cl = per_req * p.B < by_rows ? per_req * p.B : by_rows;
+        s.grid = dim3((unsigned)(n_cl * kCluster), p.Hk, p.num_splits);
+    } else {
+        s.grid = dim3((qtiles + kCluster - 1) / kCluster * kCluster, p.Hk, p.B * p.num_splits);
+    }
     s.block = 384;
     s.smem = p.D == 128 ? prefill_smem_bytes<128>() : prefill_smem_bytes<64>();
     s.nstage = p.D == 128 ? PrefillCfg<128>::kStages : PrefillCfg<64>::kStages;

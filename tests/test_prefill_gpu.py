@@ -124,3 +124,35 @@ def test_full_size_workload_on_sampled_rows(make):
     err = np.abs(got[tt, hh] - ref.forward_rows(c, tt, hh))
     assert err.max() <= 2e-2, err.max()
     assert_no_device_error()
+
+
+def test_prefill_batch_above_compact_limit():
+    """More than 256 requests: every request gets max_seqlen_q's query tiles
+    (empty clusters leave at once) instead of the compact cluster list."""
+    import paged_attention_relative_gb300 as pa
+    rng = np.random.default_rng(11)
+    sq = rng.integers(1, 41, size=300)
+    sq[0] = 40
+    sk = sq + rng.integers(0, 100, size=300)
+    c = make_case(seed=12, seqlens_q=sq.tolist(), seqlens_k=sk.tolist(), num_heads=8, num_kv_heads=2,
+                  head_dim=64, rel_extent=16)
+    got = run(c)
+    assert pa.last_launch()["kernel"] == "prefill"
+    assert pa.last_launch()["grid"][2] == 300
+    assert_close(got, ref.forward(c), what="300 requests")
+    assert_no_device_error()
+
+
+def test_prefill_compact_grid_with_inflated_max_seqlen_q():
+    """max_seqlen_q far above the longest query: the compact launch is bounded
+    by the rows (T / 64 pairs plus one per request) and still covers every pair."""
+    import paged_attention_relative_gb300 as pa
+    c = make_case(seed=13, seqlens_q=[1, 130, 0, 65, 7], seqlens_k=[300, 400, 10, 65, 900], num_heads=8,
+                  num_kv_heads=2, head_dim=128, rel_extent=40)
+    got = run(c, max_seqlen_q=8 * c.max_seqlen_q, num_splits=2)
+    info = pa.last_launch()
+    assert info["kernel"] == "prefill"
+    T = c.q.shape[0]
+    assert info["grid"][0] == 2 * ((T + 63) // 64 + 5)
+    assert_close(got, ref.forward(c), what="inflated max_seqlen_q")
+    assert_no_device_error()
