@@ -8,6 +8,9 @@ larger than the 129 MB L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
+`--workload append_chunked_prefill` times the paged KV-cache append instead
+(rel_attn_cache_append of the chunked-prefill workload's new tokens).
+
 Prints one JSON line on rank 0.  Under torchrun every rank runs its own
 replica of the workload on its own GPU (the work shards by request and kv
 head with no exchange), so scaling is weak.
@@ -294,6 +297,94 @@ def run_ours(args, rank, world):
     return res, case
 
 
+def run_append(args, rank, world):
+    """The paged KV-cache append for the chunked-prefill workload's new tokens
+    (4 x 4096 tokens, 8 kv heads, head_dim 128): HBM-bound, so `value` is
+    algorithmic bytes (key and value rows read once and written once) per
+    kernel second; L2 is flushed (a 256 MB buffer read) before every launch since the
+    rows (67 MB) fit in L2."""
+    import torch
+
+    import paged_attention_relative_gb300 as pa
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    case = make_workload("chunked_prefill")
+    d = case.dims
+    gen = torch.Generator().manual_seed(0)
+    key = torch.randn(d["T"], d["Hk"], d["D"], generator=gen).to(torch.bfloat16)
+    value = torch.randn(d["T"], d["Hk"], d["D"], generator=gen).to(torch.bfloat16)
+    g = {k: getattr(case, k).to(dev) for k in ("key_cache", "value_cache", "block_table", "cache_seqlens",
+                                               "cu_seqlens_q")}
+    kd, vd = key.to(dev), value.to(dev)
+    flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)  # 256 MB, read (clean lines) before each launch
+    stream = torch.cuda.current_stream(dev)
+
+    def call(k, v):
+        pa.rel_attn_cache_append(k, v, g["key_cache"], g["value_cache"], g["block_table"], g["cache_seqlens"],
+                                 g["cu_seqlens_q"])
+
+    for _ in range(max(args.warmup, 3)):
+        call(kd, vd)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(dev.index) as clocks:
+        for b, e in evs:
+            flush.sum()
+            b.record(stream)
+            call(kd, vd)
+            e.record(stream)
+        torch.cuda.synchronize()
+    kern_ms = sum(b.elapsed_time(e) for b, e in evs) / args.steps
+    rows = 2 * d["T"] * d["Hk"] * d["D"] * 2
+    nbytes = 2 * rows + (d["B"] + 1) * 4 + d["B"] * 4 + d["T"] * 4  # rows in and out, lengths, a table entry per token
+    pk, pk_src = peaks()
+    ach = nbytes / (kern_ms * 1e-3) / 1e9
+
+    # End to end: pinned host key/value copied in, then the append, every step.
+    hk, hv = key.pin_memory(), value.pin_memory()
+
+    def e2e_step():
+        kd.copy_(hk, non_blocking=True)
+        vd.copy_(hv, non_blocking=True)
+        call(kd, vd)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a0.elapsed_time(a1) / args.steps
+    res = {
+        "metric": "paged KV-cache append bandwidth", "value": round(world * nbytes / (kern_ms * 1e-3) / 1e12, 4),
+        "unit": "TB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(kern_ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 rows, shuffled page pool)",
+        "config": {"workload": "append_chunked_prefill", "batch": d["B"], "tokens": d["T"],
+                   "num_kv_heads": d["Hk"], "head_dim": d["D"], "block_size": d["BS"],
+                   "l2": "flushed (a 256 MB buffer read) before every launch", "algorithmic_bytes": nbytes},
+        "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(ach / pk["hbm_gbs"], 4), "traffic": None,
+                     "peak_source": f"{pk_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"},
+        "e2e": {"value": round(world * nbytes / (e2e_ms * 1e-3) / 1e12, 4), "unit": "TB/s",
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": rows, "d2h_bytes_per_step": 0,
+                "note": "pinned host key/value in, append; the product is the device cache (nothing read back)"},
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        from oracle import reference as ref
+        t0 = time.perf_counter()
+        ref.cache_append(case, key, value)
+        s = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": round(nbytes / s / 1e12, 6), "unit": "TB/s", "cores": 1, "kind": "oracle",
+                               "sample": "the whole write (every token), once", "seconds_per_step": round(s, 3)}
+    return res
+
+
 def time_oracle(case, budget_s: float):
     """The fp64 oracle on the host cores, on a bounded sample of the workload's
     output rows; returns (seconds per full workload, sample description, cores)."""
@@ -345,6 +436,14 @@ def main():
         import torch
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         torch.distributed.init_process_group("nccl")
+    if args.workload == "append_chunked_prefill":
+        res = run_append(args, rank, world)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+        return
     res, case = run_ours(args, rank, world)
     if rank == 0 and not args.no_cpu_baseline:
         full_s, sample, cores = time_oracle(case, args.cpu_budget)

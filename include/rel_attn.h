@@ -224,6 +224,56 @@ rel_attn_status rel_attn_paged_varlen_noalloc(
     rel_attn_stream stream);
 
 /*
+ * rel_attn_cache_append - write the new tokens' keys and values into the paged
+ * caches, the step before attending over them.  The attention of
+ * inkling_fa4_rel_attention (vLLM API docs) reads cache_seqlens keys per
+ * request and aligns query row i at key position i + cache_seqlens[b] - sq_b
+ * (bottom-right), so the new tokens are the last sq_b keys of the cache and
+ * must be in it before the call.  The pages show no interface for that write,
+ * so this one reuses the attention's arguments: token i of
+ * request b (row t = cu_seqlens_q[b] + i) is the key at logical position
+ * pos = cache_seqlens[b] - sq_b + i, the bottom-right position the attention
+ * gives it, and
+ *
+ *   key_cache[block_table[b, pos / BS], pos % BS, h, :] = key[t, h, :]
+ *   value_cache[...same slot...]                        = value[t, h, :]
+ *
+ * for every kv head h.  A token with pos < 0 (cache_seqlens[b] < sq_b) has no
+ * slot and is not written.  Bits are copied unchanged.
+ *
+ * Arguments (device tensors, current device, sm_103):
+ *   key, value     (T, Hk, D) bf16; last dim contiguous, base and strides
+ *                  16-byte multiples; read only
+ *   key_cache, value_cache
+ *                  (NB, BS, Hk, D) bf16 as for rel_attn_paged_varlen; written
+ *   block_table, cache_seqlens, cu_seqlens_q
+ *                  as for rel_attn_paged_varlen (cache_seqlens already counts
+ *                  the new tokens)
+ *   stream         the stream the copy is ordered on
+ *
+ * Supported: D a multiple of 8 up to 512; any BS > 0.
+ * Ownership: all tensors caller-owned, borrowed until the stream work
+ * completes; nothing is allocated.  The slots written must be distinct (block
+ * tables of different requests must not share a slot in the written range);
+ * otherwise which write lands is unspecified.
+ * Errors: REL_ATTN_ERR_INVALID_ARGUMENT for a NULL pointer with a nonzero size,
+ * a dtype/rank/shape/stride mismatch, or key/value overlapping a cache;
+ * REL_ATTN_ERR_UNSUPPORTED for a D it cannot copy, misaligned data or a device
+ * that is not sm_103; REL_ATTN_ERR_CUDA for a launch error.  T == 0 is a
+ * no-op.  Device-side preconditions as for rel_attn_paged_varlen (checked when
+ * REL_ATTN_CHECK=1).
+ */
+rel_attn_status rel_attn_cache_append(
+    const rel_attn_tensor* key,
+    const rel_attn_tensor* value,
+    rel_attn_tensor* key_cache,
+    rel_attn_tensor* value_cache,
+    const rel_attn_tensor* block_table,
+    const rel_attn_tensor* cache_seqlens,
+    const rel_attn_tensor* cu_seqlens_q,
+    rel_attn_stream stream);
+
+/*
  * rel_attn_num_splits - split-KV cap for this attention, defined by
  * inkling_fa4_num_splits (vLLM API docs, fa4_rel_attention) without its
  * Hopper branch (this library runs on sm_103 only).  Local (windowed)

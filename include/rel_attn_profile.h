@@ -18,7 +18,8 @@ extern "C" {
 typedef enum {
     REL_ATTN_KERNEL_NONE = 0,
     REL_ATTN_KERNEL_DECODE = 1,   /* split-KV decode kernel, <= 64 packed rows  */
-    REL_ATTN_KERNEL_PREFILL = 2   /* tcgen05 prefill kernel, 128-row tiles      */
+    REL_ATTN_KERNEL_PREFILL = 2,  /* tcgen05 prefill kernel, 128-row tiles      */
+    REL_ATTN_KERNEL_APPEND = 3    /* paged KV-cache append (rel_attn_cache_append) */
 } rel_attn_kernel_kind;
 
 /* What the last rel_attn_paged_varlen call on this thread launched. */

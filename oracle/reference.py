@@ -170,6 +170,37 @@ def brute_force(c, with_lse: bool = False):
     return (o, np.array(lse, dtype=np.float64).reshape(T, H)) if with_lse else o
 
 
+def cache_append(c, key: torch.Tensor, value: torch.Tensor):
+    """New (key_cache, value_cache) after writing the new tokens' rows.
+
+    Token i of request b (row t = cu_seqlens_q[b] + i) is the key at logical
+    position pos = cache_seqlens[b] - sq_b + i: the bottom-right position the
+    attention of inkling_fa4_rel_attention (vLLM API docs) gives query row i,
+    so the new tokens are the last sq_b keys of the request.  Its row goes to
+    slot pos % BS of physical block block_table[b, pos // BS] for every kv
+    head; tokens with pos < 0 have no slot and are skipped.  Plain loops over
+    requests and tokens; the inputs are not modified.
+    """
+    kc = c.key_cache.detach().cpu().clone()
+    vc = c.value_cache.detach().cpu().clone()
+    key = key.detach().cpu()
+    value = value.detach().cpu()
+    table = c.block_table.tolist()
+    seqk = c.cache_seqlens.tolist()
+    cu = c.cu_seqlens_q.tolist()
+    BS = kc.shape[1]
+    for b in range(len(seqk)):
+        n_new = cu[b + 1] - cu[b]
+        for i in range(n_new):
+            pos = seqk[b] - n_new + i
+            if pos < 0:
+                continue
+            blk, slot = table[b][pos // BS], pos % BS
+            kc[blk, slot] = key[cu[b] + i]
+            vc[blk, slot] = value[cu[b] + i]
+    return kc, vc
+
+
 # ---------------------------------------------------------------------------
 # Split-count heuristic and scheduling-bound bucketing, restated from the vLLM
 # API docs for vllm.models.inkling.nvidia.ops.fa4_rel_attention

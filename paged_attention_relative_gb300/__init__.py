@@ -9,7 +9,7 @@ from __future__ import annotations
 
 
 def __getattr__(name):
-    if name in ("rel_attn_paged_varlen", "rel_attn_paged_varlen_lse", "rel_attn_paged_varlen_noalloc", "rel_attn_num_splits",
+    if name in ("rel_attn_paged_varlen", "rel_attn_paged_varlen_lse", "rel_attn_paged_varlen_noalloc", "rel_attn_cache_append", "rel_attn_num_splits",
                 "rel_attn_bucket_max_seqlen_q", "last_launch", "set_kernel_events", "device_error", "RelAttnError",
                 "describe"):
         from . import _lib
@@ -17,5 +17,5 @@ def __getattr__(name):
     raise AttributeError(name)
 
 
-__all__ = ["rel_attn_paged_varlen", "rel_attn_paged_varlen_lse", "rel_attn_paged_varlen_noalloc", "rel_attn_num_splits",
+__all__ = ["rel_attn_paged_varlen", "rel_attn_paged_varlen_lse", "rel_attn_paged_varlen_noalloc", "rel_attn_cache_append", "rel_attn_num_splits",
            "rel_attn_bucket_max_seqlen_q", "last_launch", "set_kernel_events", "device_error", "RelAttnError"]

@@ -18,10 +18,11 @@ LIB_PATH = os.path.join(HERE, "librel_attn.so")
 
 REL_ATTN_BF16, REL_ATTN_F32, REL_ATTN_I32 = 0, 1, 2
 STATUS = {0: "OK", 1: "INVALID_ARGUMENT", 2: "UNSUPPORTED", 3: "CUDA", 4: "OUT_OF_MEMORY", 5: "DEVICE_CHECK"}
-KERNELS = {0: "none", 1: "decode", 2: "prefill"}
+KERNELS = {0: "none", 1: "decode", 2: "prefill", 3: "append"}
 
 # Every function the headers declare, with its ctypes signature.
 EXPORTS = ("rel_attn_paged_varlen", "rel_attn_paged_varlen_lse", "rel_attn_paged_varlen_noalloc", "rel_attn_num_splits",
+           "rel_attn_cache_append",
            "rel_attn_bucket_max_seqlen_q",
            "rel_attn_last_error", "rel_attn_last_launch", "rel_attn_set_kernel_events", "rel_attn_device_error")
 
@@ -57,6 +58,8 @@ def _load() -> ctypes.CDLL:
     lib.rel_attn_paged_varlen_lse.restype = ctypes.c_int
     lib.rel_attn_paged_varlen_noalloc.argtypes = lib.rel_attn_paged_varlen.argtypes
     lib.rel_attn_paged_varlen_noalloc.restype = ctypes.c_int
+    lib.rel_attn_cache_append.argtypes = [P, P, P, P, P, P, P, ctypes.c_void_p]
+    lib.rel_attn_cache_append.restype = ctypes.c_int
     lib.rel_attn_num_splits.argtypes = [i32] * 6
     lib.rel_attn_num_splits.restype = i32
     lib.rel_attn_bucket_max_seqlen_q.argtypes = [i32]
@@ -171,6 +174,18 @@ def rel_attn_paged_varlen_noalloc(q, key_cache, value_cache, block_table, cache_
                                            ctypes.c_void_p(stream))
     _check(st)
     return out
+
+
+def rel_attn_cache_append(key, value, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_q,
+                          stream=None):
+    """Write the new tokens' key/value rows into the paged caches; see include/rel_attn.h."""
+    if stream is None:
+        stream = torch.cuda.current_stream(key.device).cuda_stream
+    elif isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    d = [describe(t) for t in (key, value, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_q)]
+    _check(lib.rel_attn_cache_append(*[_ref(x) for x in d], ctypes.c_void_p(stream)))
+    return key_cache, value_cache
 
 
 def rel_attn_num_splits(is_local, batch_size, max_query_len, num_heads, num_kv_heads, max_kv_len) -> int:

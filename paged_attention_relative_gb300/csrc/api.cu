@@ -548,3 +548,113 @@ int* device_error_word() {
 }
 
 }  // namespace relattn
+
+extern "C" rel_attn_status rel_attn_cache_append(
+    const rel_attn_tensor* key, const rel_attn_tensor* value, rel_attn_tensor* key_cache,
+    rel_attn_tensor* value_cache, const rel_attn_tensor* block_table, const rel_attn_tensor* cache_seqlens,
+    const rel_attn_tensor* cu_seqlens_q, rel_attn_stream stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    t_launch = rel_attn_launch_info{};
+    rel_attn_status st;
+    if ((st = check_tensor(key, "key", REL_ATTN_BF16, 3))) return st;
+    if ((st = check_tensor(value, "value", REL_ATTN_BF16, 3))) return st;
+    if ((st = check_tensor(key_cache, "key_cache", REL_ATTN_BF16, 4))) return st;
+    if ((st = check_tensor(value_cache, "value_cache", REL_ATTN_BF16, 4))) return st;
+    if ((st = check_tensor(block_table, "block_table", REL_ATTN_I32, 2))) return st;
+    if ((st = check_tensor(cache_seqlens, "cache_seqlens", REL_ATTN_I32, 1))) return st;
+    if ((st = check_tensor(cu_seqlens_q, "cu_seqlens_q", REL_ATTN_I32, 1))) return st;
+    const int64_t T = key->shape[0], Hk = key->shape[1], D = key->shape[2];
+    const int64_t NB = key_cache->shape[0], BS = key_cache->shape[1];
+    const int64_t B = block_table->shape[0], MB = block_table->shape[1];
+    for (int i = 0; i < 3; ++i)
+        if (value->shape[i] != key->shape[i]) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "value shape differs from key");
+    for (int i = 0; i < 4; ++i) {
+        if (value_cache->shape[i] != key_cache->shape[i])
+            return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "value_cache shape differs from key_cache");
+        if (value_cache->stride[i] != key_cache->stride[i])
+            return fail(REL_ATTN_ERR_UNSUPPORTED, "value_cache strides must equal key_cache strides");
+    }
+    if (key_cache->shape[2] != Hk || key_cache->shape[3] != D)
+        return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "key is (T, Hk, D) with the caches' Hk and D");
+    if (cache_seqlens->shape[0] != B) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "cache_seqlens must have B entries");
+    if (cu_seqlens_q->shape[0] != B + 1) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "cu_seqlens_q must have B+1 entries");
+    if (cache_seqlens->stride[0] != 1 || cu_seqlens_q->stride[0] != 1)
+        return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "cache_seqlens and cu_seqlens_q must be contiguous");
+    if (MB > 0 && block_table->stride[1] != 1)
+        return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "block_table rows must be contiguous");
+    if (B > 0 && block_table->stride[0] < MB)
+        return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "block_table row stride smaller than its width");
+    if (key->stride[2] != 1 || value->stride[2] != 1 || key_cache->stride[3] != 1)
+        return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "the head_dim axis must be contiguous");
+    if (D <= 0 || D % 8 != 0 || D > 512) return fail(REL_ATTN_ERR_UNSUPPORTED, "head_dim must be a multiple of 8 up to 512");
+    if (BS <= 0) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "block_size must be positive");
+    if (T > INT32_MAX / 2 || NB > INT32_MAX || B > INT32_MAX / 2)
+        return fail(REL_ATTN_ERR_UNSUPPORTED, "sizes beyond 32-bit indexing");
+    for (const rel_attn_tensor* src : {key, value})
+        for (const rel_attn_tensor* dst : {key_cache, value_cache})
+            if (overlaps(src, 2, dst, 2)) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "key/value alias a cache");
+    if (overlaps(key_cache, 2, value_cache, 2)) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "key_cache aliases value_cache");
+    if (T == 0 || B == 0) {
+        t_launch.kernel = REL_ATTN_KERNEL_NONE;
+        return REL_ATTN_OK;
+    }
+    for (const rel_attn_tensor* c : {key, value})
+        if (!aligned(c->data, 16) || c->stride[0] % 8 || c->stride[1] % 8)
+            return fail(REL_ATTN_ERR_UNSUPPORTED, "key/value need 16-byte aligned bases and strides");
+    for (const rel_attn_tensor* c : {key_cache, value_cache})
+        if (!aligned(c->data, 16) || c->stride[0] % 8 || c->stride[1] % 8 || c->stride[2] % 8)
+            return fail(REL_ATTN_ERR_UNSUPPORTED, "caches need 16-byte aligned bases and strides");
+
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev))) return st;
+    if (dev->major != 10 || dev->minor != 3)
+        return fail(REL_ATTN_ERR_UNSUPPORTED, "built for sm_103a; device is sm_%d%d", dev->major, dev->minor);
+    if (check_enabled()) {
+        cudaError_t e = cudaMemsetAsync(dev->check_err, 0, sizeof(int), stream);
+        if (e == cudaSuccess) {
+            check_kernel<<<(unsigned)((B + 127) / 128), 128, 0, stream>>>(
+                static_cast<const int32_t*>(cu_seqlens_q->data), static_cast<const int32_t*>(cache_seqlens->data),
+                static_cast<const int32_t*>(block_table->data), block_table->stride[0], (int)B, (int)T, (int)MB,
+                (int)BS, (int)NB, (int)T, dev->check_err);
+            e = cudaGetLastError();
+        }
+        int code = 0;
+        if (e == cudaSuccess) e = cudaMemcpyAsync(&code, dev->check_err, sizeof code, cudaMemcpyDeviceToHost, stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+        if (e != cudaSuccess) return fail(REL_ATTN_ERR_CUDA, "check kernel: %s", cudaGetErrorString(e));
+        if (code) return fail(REL_ATTN_ERR_DEVICE_CHECK, "device-side precondition violated (code %d)", code);
+    }
+    AppendParams p{};
+    p.key = key->data;
+    p.value = value->data;
+    p.k_st = key->stride[0];
+    p.k_sh = key->stride[1];
+    p.v_st = value->stride[0];
+    p.v_sh = value->stride[1];
+    p.k_cache = key_cache->data;
+    p.v_cache = value_cache->data;
+    p.c_s0 = key_cache->stride[0];
+    p.c_s1 = key_cache->stride[1];
+    p.c_s2 = key_cache->stride[2];
+    p.block_table = static_cast<const int32_t*>(block_table->data);
+    p.bt_stride = block_table->stride[0];
+    p.cache_seqlens = static_cast<const int32_t*>(cache_seqlens->data);
+    p.cu_seqlens_q = static_cast<const int32_t*>(cu_seqlens_q->data);
+    p.B = (int32_t)B;
+    p.T = (int32_t)T;
+    p.Hk = (int32_t)Hk;
+    p.BS = (int32_t)BS;
+    p.D = (int32_t)D;
+    if (t_ev_begin) cudaEventRecord(t_ev_begin, stream);
+    cudaError_t e = launch_append(p, stream);
+    if (t_ev_end) cudaEventRecord(t_ev_end, stream);
+    t_launch.kernel = REL_ATTN_KERNEL_APPEND;
+    t_launch.num_splits = 0;
+    t_launch.grid[0] = (int32_t)((T + 7) / 8);
+    t_launch.grid[1] = 1;
+    t_launch.grid[2] = 1;
+    t_launch.block = 256;
+    t_launch.launches = 1;
+    if (e != cudaSuccess) return fail(REL_ATTN_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+    return REL_ATTN_OK;
+}

@@ -68,6 +68,22 @@ int prefill_bias_window();
 cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap* maps, const LaunchShape& shape,
                            cudaStream_t stream);
 
+// Paged KV-cache append (key/value rows of the new tokens into the caches).
+struct AppendParams {
+    const void* key;           // (T, Hk, D) bf16
+    const void* value;
+    int64_t k_st, k_sh, v_st, v_sh;  // token / head strides
+    void* k_cache;             // (NB, BS, Hk, D) bf16
+    void* v_cache;
+    int64_t c_s0, c_s1, c_s2;  // cache block / slot / head strides (shared by K and V)
+    const int32_t* block_table;
+    int64_t bt_stride;
+    const int32_t* cache_seqlens;
+    const int32_t* cu_seqlens_q;
+    int32_t B, T, Hk, BS, D;
+};
+cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
+
 // LSE-weighted merge of split partials into out (and lse when requested).
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t stream);
 

@@ -184,3 +184,18 @@ def test_lse_argument_is_validated_before_device_work(make_lse):
                                     c.cu_seqlens_q, c.max_seqlen_q, c.softmax_scale, c.causal, -1, -1,
                                     c.rel_extent, c.rel_logits, 1, out=out, softmax_lse=make_lse(c, out), stream=0)
     assert ei.value.status == 1
+
+
+@pytest.mark.parametrize("what", ["shape", "alias"])
+def test_cache_append_validates_before_device_work(what):
+    L = _lib()
+    c = _cpu_case()
+    T, Hk, D = c.q.shape[0], c.key_cache.shape[2], c.key_cache.shape[3]
+    key = torch.zeros(T, Hk + 1, D, dtype=torch.bfloat16) if what == "shape" else c.key_cache[0, :T]
+    value = torch.zeros(T, Hk, D, dtype=torch.bfloat16)
+    if what == "alias":
+        key = c.value_cache.view(-1, Hk, D)[:T]
+    with pytest.raises(L.RelAttnError) as ei:
+        L.rel_attn_cache_append(key, value, c.key_cache, c.value_cache, c.block_table, c.cache_seqlens,
+                                c.cu_seqlens_q, stream=0)
+    assert ei.value.status == 1

@@ -307,3 +307,70 @@ def test_num_splits_matches_worked_values():
 def test_bucket_max_seqlen_q_matches_worked_values():
     for n, want in _golden("bucket_max_seqlen_q.txt"):
         assert ref.bucket_max_seqlen_q(n) == want
+
+
+# --------------------------------------------------------------------- cache append
+
+def _new_rows(c, seed):
+    g = torch.Generator().manual_seed(seed)
+    T, Hk, D = c.q.shape[0], c.key_cache.shape[2], c.key_cache.shape[3]
+    k = torch.randn(T, Hk, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(T, Hk, D, generator=g).to(torch.bfloat16)
+    return k, v
+
+
+def test_cache_append_round_trip_through_block_table():
+    """Reading the request's last sq keys back through the (permuted) block
+    table returns the appended rows bit for bit; every other slot is unchanged."""
+    c = _small(40, seqlens_q=[3, 0, 5], seqlens_k=[9, 4, 13])
+    key, value = _new_rows(c, 1)
+    kc, vc = ref.cache_append(c, key, value)
+    c2 = c.with_(key_cache=kc, value_cache=vc)
+    cu = c.cu_seqlens_q.tolist()
+    written = torch.zeros(kc.shape[:2], dtype=torch.bool)
+    for b in range(3):
+        sq, sk = cu[b + 1] - cu[b], int(c.cache_seqlens[b])
+        got_k = _kv_contig(c2, b, "k")[sk - sq:]
+        got_v = _kv_contig(c2, b, "v")[sk - sq:]
+        assert torch.equal(got_k, key[cu[b]:cu[b + 1]].double())
+        assert torch.equal(got_v, value[cu[b]:cu[b + 1]].double())
+        assert torch.equal(_kv_contig(c2, b, "k")[:sk - sq], _kv_contig(c, b, "k")[:sk - sq])
+        for pos in range(sk - sq, sk):
+            written[int(c.block_table[b, pos // 4]), pos % 4] = True
+    assert torch.equal(kc[~written], c.key_cache[~written])
+    assert torch.equal(vc[~written], c.value_cache[~written])
+
+
+def test_cache_append_skips_tokens_without_a_slot():
+    """sk < sq: the first sq - sk tokens have negative positions and write nothing."""
+    c = _small(41, seqlens_q=[5], seqlens_k=[2])
+    key, value = _new_rows(c, 2)
+    kc, _ = ref.cache_append(c, key, value)
+    got = _kv_contig(c.with_(key_cache=kc), 0, "k")
+    assert torch.equal(got, key[3:5].double())
+    untouched = torch.ones(kc.shape[:2], dtype=torch.bool)
+    untouched[int(c.block_table[0, 0]), 0:2] = False
+    assert torch.equal(kc[untouched], c.key_cache[untouched])
+
+
+def test_append_then_attend_equals_sdpa_over_prefix_and_new_rows():
+    """Appended rows are the keys the attention aligns with the new tokens:
+    with zero bias, attending over the cache equals SDPA over [prefix, new]
+    with torch's lower-right causal mask."""
+    c = _small(42, seqlens_q=[4, 6], seqlens_k=[11, 6], rel_extent=0, head_dim=16)
+    key, value = _new_rows(c, 3)
+    kc, vc = ref.cache_append(c, key, value)
+    c2 = c.with_(key_cache=kc, value_cache=vc)
+    out = ref.forward(c2)
+    cu = c.cu_seqlens_q.tolist()
+    G = c.q.shape[1] // c.key_cache.shape[2]
+    for b in range(2):
+        sq, sk = cu[b + 1] - cu[b], int(c.cache_seqlens[b])
+        k_all = torch.cat([_kv_contig(c, b, "k")[:sk - sq], key[cu[b]:cu[b + 1]].double()])
+        v_all = torch.cat([_kv_contig(c, b, "v")[:sk - sq], value[cu[b]:cu[b + 1]].double()])
+        q = c.q[cu[b]:cu[b + 1]].double().transpose(0, 1)                 # (H, sq, D)
+        k = k_all.transpose(0, 1).repeat_interleave(G, 0)                  # (H, sk, D)
+        v = v_all.transpose(0, 1).repeat_interleave(G, 0)
+        want = F.scaled_dot_product_attention(q, k, v, attn_mask=causal_lower_right(sq, sk),
+                                              scale=float(np.float32(c.softmax_scale)))
+        np.testing.assert_allclose(out[cu[b]:cu[b + 1]], want.transpose(0, 1).numpy(), rtol=0, atol=1e-12)
