@@ -124,6 +124,24 @@ class ClockSampler:
                 "power_w_max": max(r["power"] for r in rows)}
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of every rank's x (the job's time is its slowest rank's):
+    an all-reduce on `device` (a CUDA device under NCCL, CPU under gloo)."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, work_per_replica: float, ms: float) -> float:
+    """Whole-job throughput in work units per second x 1e-12: every rank runs
+    one replica of the workload, so the job did world x the work in the
+    slowest rank's time."""
+    return world * work_per_replica / (ms * 1e-3) / 1e12
+
+
 def make_workload(name: str):
     from paged_attention_relative_gb300 import workloads as W
     return W.WORKLOADS[name](0)
@@ -196,11 +214,7 @@ def run_ours(args, rank, world):
         e1.record(stream)
         torch.cuda.synchronize()
     barrier()
-    ms_total = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(e0.elapsed_time(e1), world, dev)
     ms_step = ms_total / args.steps
 
     # Main-kernel timing with events recorded by the library around the launch.
@@ -245,20 +259,16 @@ def run_ours(args, rank, world):
         e2e_step()
     a1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = a0.elapsed_time(a1) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(a0.elapsed_time(a1) / args.steps, world, dev)
 
     nbytes = algorithmic_bytes(case)
     flops = algorithmic_flops(case)
     pk, pk_src = peaks()
     decode = kind == "decode"
     if decode:
-        value = world * nbytes / (ms_step * 1e-3) / 1e12
+        value = job_rate(world, nbytes, ms_step)
         unit = "TB/s"
-        e2e_value = world * nbytes / (e2e_ms * 1e-3) / 1e12
+        e2e_value = job_rate(world, nbytes, e2e_ms)
         ach = nbytes / (kern_avg * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(ach / pk["hbm_gbs"], 4), "traffic": recorded_traffic(args.workload, kind),
@@ -266,9 +276,9 @@ def run_ours(args, rank, world):
                 if pk_src == "measured" else "fallback 6.8 TB/s",
                 "nominal_frac_8tbs": round(ach / 8000.0, 4)}
     else:
-        value = world * flops / (ms_step * 1e-3) / 1e12
+        value = job_rate(world, flops, ms_step)
         unit = "TFLOP/s"
-        e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+        e2e_value = job_rate(world, flops, e2e_ms)
         ach = flops / (kern_avg * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(ach / pk["bf16_tflops"], 4), "traffic": recorded_traffic(args.workload, kind),
@@ -335,7 +345,7 @@ def run_append(args, rank, world):
             call(kd, vd)
             e.record(stream)
         torch.cuda.synchronize()
-    kern_ms = sum(b.elapsed_time(e) for b, e in evs) / args.steps
+    kern_ms = max_over_ranks(sum(b.elapsed_time(e) for b, e in evs) / args.steps, world, dev)
     rows = 2 * d["T"] * d["Hk"] * d["D"] * 2
     nbytes = 2 * rows + (d["B"] + 1) * 4 + d["B"] * 4 + d["T"] * 4  # rows in and out, lengths, a table entry per token
     pk, pk_src = peaks()
@@ -357,9 +367,9 @@ def run_append(args, rank, world):
         e2e_step()
     a1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = a0.elapsed_time(a1) / args.steps
+    e2e_ms = max_over_ranks(a0.elapsed_time(a1) / args.steps, world, dev)
     res = {
-        "metric": "paged KV-cache append bandwidth", "value": round(world * nbytes / (kern_ms * 1e-3) / 1e12, 4),
+        "metric": "paged KV-cache append bandwidth", "value": round(job_rate(world, nbytes, kern_ms), 4),
         "unit": "TB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(kern_ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 rows, shuffled page pool)",
@@ -369,7 +379,7 @@ def run_append(args, rank, world):
         "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": round(ach / pk["hbm_gbs"], 4), "traffic": None,
                      "peak_source": f"{pk_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"},
-        "e2e": {"value": round(world * nbytes / (e2e_ms * 1e-3) / 1e12, 4), "unit": "TB/s",
+        "e2e": {"value": round(job_rate(world, nbytes, e2e_ms), 4), "unit": "TB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": rows, "d2h_bytes_per_step": 0,
                 "note": "pinned host key/value in, append; the product is the device cache (nothing read back)"},
         "gpu_launches": args.steps,
