@@ -395,13 +395,14 @@ def run_append(args, rank, world):
     return res
 
 
-def time_oracle(case, budget_s: float):
-    """The fp64 oracle on the host cores, on a bounded sample of the workload's
-    output rows; returns (seconds per full workload, sample description, cores)."""
+def time_oracle(case, budget_s: float, cores: int | None = None):
+    """The fp64 oracle on the host cores (all of them unless `cores` is given),
+    on a bounded sample of the workload's output rows; returns (seconds per
+    full workload, sample description, cores)."""
     import numpy as np
 
     from oracle import reference as ref
-    cores = ref.default_threads()
+    cores = cores or ref.default_threads()
     d = case.dims
     T, H = d["T"], d["H"]
     n_rows = T * H
@@ -460,6 +461,9 @@ def main():
         unit_work = res["config"]["algorithmic_bytes"] if res["unit"] == "TB/s" else res["config"]["algorithmic_flops"]
         res["cpu_baseline"] = {"value": round(unit_work / full_s / 1e12, 6), "unit": res["unit"], "cores": cores,
                                "kind": "oracle", "sample": sample, "seconds_per_step": round(full_s, 3)}
+        one_s, one_sample, _ = time_oracle(case, min(4.0, args.cpu_budget), cores=1)
+        res["cpu_baseline"]["single_core"] = {"value": round(unit_work / one_s / 1e12, 6), "cores": 1,
+                                              "sample": one_sample, "seconds_per_step": round(one_s, 3)}
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

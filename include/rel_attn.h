@@ -87,8 +87,11 @@ typedef enum {
  *                  sliding window in keys; a negative side is unbounded;
  *                  (-1, -1) means no window
  *   rel_extent     R >= 0; R == 0 means no bias (rel_logits may then be NULL)
- *   rel_logits     (T, H, R) bf16, fully contiguous (the pages make the bias
- *                  tensor contiguous before the call)
+ *   rel_logits     (T, H, R) bf16 or fp32, fully contiguous (the pages make the
+ *                  bias tensor contiguous before the call); bf16 rows with
+ *                  R % 8 == 0 are staged by TMA on the prefill path, other
+ *                  rows (fp32, or an R that is not a multiple of 8) are read
+ *                  per element
  *   num_splits     >= 1: a cap on the number of KV splits per (request, kv head);
  *                  1 writes out directly, >1 writes fp32 partials and runs an
  *                  LSE-weighted combine.  Clamped to what the KV length allows.

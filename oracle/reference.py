@@ -32,7 +32,7 @@ def _load():
         I64 = ctypes.c_int64
         I = ctypes.c_int
         D = ctypes.c_double
-        common = [P, P, P, P, I64, P, P, I64, I64, I64, I64, I64, I64, I64, D, I, I, I, I64, P]
+        common = [P, P, P, P, I64, P, P, I64, I64, I64, I64, I64, I64, I64, D, I, I, I, I64, P, I]
         lib.rel_attn_oracle_forward.argtypes = common + [P, P, I]
         lib.rel_attn_oracle_forward.restype = I
         lib.rel_attn_oracle_rows.argtypes = common + [I64, P, P, P, I]
@@ -61,8 +61,9 @@ def _common_args(c):
     NB, BS, Hk, _ = c.key_cache.shape
     B = bt.shape[0]
     R = int(c.rel_extent)
+    rel_f32 = R > 0 and c.rel_logits.dtype == torch.float32
     if R > 0:
-        rel = _bits(c.rel_logits)
+        rel = (np.ascontiguousarray(c.rel_logits.detach().cpu().numpy()) if rel_f32 else _bits(c.rel_logits))
         assert rel.size == T * H * R
     else:
         rel = np.zeros(1, dtype=np.uint16)
@@ -71,7 +72,7 @@ def _common_args(c):
     scale = float(np.float32(c.softmax_scale))
     args = [q.ctypes.data, kc.ctypes.data, vc.ctypes.data, bt.ctypes.data, bt.shape[1],
             sk.ctypes.data, cu.ctypes.data, B, T, H, Hk, D, NB, BS, scale,
-            int(bool(c.causal)), int(c.window_left), int(c.window_right), R, rel.ctypes.data]
+            int(bool(c.causal)), int(c.window_left), int(c.window_right), R, rel.ctypes.data, int(rel_f32)]
     return args, keep
 
 

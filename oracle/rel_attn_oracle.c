@@ -48,6 +48,11 @@ static double bf16_to_f64(uint16_t bits) {
     return (double)f;
 }
 
+/* rel_logits[idx] as a double: bf16 bits or an fp32 value, both exact. */
+static double rel_value(const void* rel, int is_f32, int64_t idx) {
+    return is_f32 ? (double)((const float*)rel)[idx] : bf16_to_f64(((const uint16_t*)rel)[idx]);
+}
+
 /* Is key j visible from row i of a request with offset off = sk - sq? */
 static int key_allowed(int64_t i, int64_t j, int64_t off, int causal, int wl, int wr) {
     int64_t d = i + off - j;
@@ -93,7 +98,7 @@ int rel_attn_oracle_forward(
     const int32_t* cache_seqlens, const int32_t* cu_seqlens_q,
     int64_t B, int64_t T, int64_t H, int64_t Hk, int64_t D, int64_t NB, int64_t BS,
     double softmax_scale, int causal, int window_left, int window_right,
-    int64_t rel_extent, const uint16_t* rel_logits,
+    int64_t rel_extent, const void* rel_logits, int rel_is_f32,
     double* out, double* lse, int num_threads) {
     if (B < 0 || T < 0 || H <= 0 || Hk <= 0 || D <= 0 || BS <= 0 || H % Hk != 0 || rel_extent < 0)
         return 10;
@@ -137,7 +142,7 @@ int rel_attn_oracle_forward(
                 const int64_t d = i + off - j;
                 double bias = 0.0;
                 if (d >= 0 && d < rel_extent)
-                    bias = bf16_to_f64(rel_logits[(t * H + h) * rel_extent + d]);
+                    bias = rel_value(rel_logits, rel_is_f32, (t * H + h) * rel_extent + d);
                 S[i * sk + j] = softmax_scale * dot + bias;
             }
         }
@@ -181,7 +186,7 @@ int rel_attn_oracle_rows(
     const int32_t* cache_seqlens, const int32_t* cu_seqlens_q,
     int64_t B, int64_t T, int64_t H, int64_t Hk, int64_t D, int64_t NB, int64_t BS,
     double softmax_scale, int causal, int window_left, int window_right,
-    int64_t rel_extent, const uint16_t* rel_logits,
+    int64_t rel_extent, const void* rel_logits, int rel_is_f32,
     int64_t n, const int64_t* row_t, const int64_t* row_h, double* out_rows, int num_threads) {
     if (B < 0 || T < 0 || H <= 0 || Hk <= 0 || D <= 0 || BS <= 0 || H % Hk != 0 || rel_extent < 0)
         return 10;
@@ -221,7 +226,7 @@ int rel_attn_oracle_rows(
                 dot += bf16_to_f64(q[(t * H + h) * D + k]) * bf16_to_f64(kr[k]);
             const int64_t d = i + off - j;
             double bias = 0.0;
-            if (d >= 0 && d < rel_extent) bias = bf16_to_f64(rel_logits[(t * H + h) * rel_extent + d]);
+            if (d >= 0 && d < rel_extent) bias = rel_value(rel_logits, rel_is_f32, (t * H + h) * rel_extent + d);
             s[j] = softmax_scale * dot + bias;
             if (s[j] > m) m = s[j];
         }

@@ -329,8 +329,10 @@ rel_attn_status paged_varlen(
     if (num_splits < 1) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "num_splits must be >= 1 (got %d)", num_splits);
     if (rel_extent < 0) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "rel_extent must be >= 0 (got %d)", rel_extent);
     if (max_seqlen_q < 0) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "max_seqlen_q must be >= 0");
+    const bool rel_f32 = rel_extent > 0 && rel_logits && rel_logits->dtype == REL_ATTN_F32;
+    const int rel_elem = rel_f32 ? 4 : 2;
     if (rel_extent > 0) {
-        if ((st = check_tensor(rel_logits, "rel_logits", REL_ATTN_BF16, 3))) return st;
+        if ((st = check_tensor(rel_logits, "rel_logits", rel_f32 ? REL_ATTN_F32 : REL_ATTN_BF16, 3))) return st;
         if (rel_logits->shape[0] != T || rel_logits->shape[1] != H || rel_logits->shape[2] != rel_extent)
             return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "rel_logits must be (T, H, rel_extent)");
         if (rel_logits->stride[2] != 1 || rel_logits->stride[1] != rel_extent ||
@@ -347,7 +349,7 @@ rel_attn_status paged_varlen(
         return fail(REL_ATTN_ERR_UNSUPPORTED, "sizes beyond 32-bit indexing");
     if (T > 0 && max_seqlen_q < 1) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "max_seqlen_q must be >= 1 when T > 0");
     if (overlaps(out, out_elem, q, 2) || overlaps(out, out_elem, key_cache, 2) ||
-        overlaps(out, out_elem, value_cache, 2) || (rel_extent > 0 && overlaps(out, out_elem, rel_logits, 2)))
+        overlaps(out, out_elem, value_cache, 2) || (rel_extent > 0 && overlaps(out, out_elem, rel_logits, rel_elem)))
         return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "out aliases an input");
     if (lse) {
         if ((st = check_tensor(lse, "softmax_lse", REL_ATTN_F32, 2))) return st;
@@ -358,7 +360,7 @@ rel_attn_status paged_varlen(
         if (overlaps(lse, 4, q, 2) || overlaps(lse, 4, key_cache, 2) || overlaps(lse, 4, value_cache, 2) ||
             overlaps(lse, 4, block_table, 4) || overlaps(lse, 4, cache_seqlens, 4) ||
             overlaps(lse, 4, cu_seqlens_q, 4) || overlaps(lse, 4, out, out_elem) ||
-            (rel_extent > 0 && overlaps(lse, 4, rel_logits, 2)))
+            (rel_extent > 0 && overlaps(lse, 4, rel_logits, rel_elem)))
             return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "softmax_lse aliases an input or out");
         if (!aligned(lse->data, 4)) return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "softmax_lse is not 4-byte aligned");
     }
@@ -421,7 +423,9 @@ rel_attn_status paged_varlen(
     p.cu_seqlens_q = static_cast<const int32_t*>(cu_seqlens_q->data);
     p.rel = rel_extent > 0 ? rel_logits->data : nullptr;
     p.R = rel_extent;
-    p.vec_bias = (rel_extent > 0 && rel_extent % 8 == 0 && aligned(rel_logits->data, 16)) ? 1 : 0;
+    p.bias_f32 = rel_f32 ? 1 : 0;
+    // bf16 bias windows are staged by TMA; fp32 rel_logits are read per element.
+    p.vec_bias = (rel_extent > 0 && !rel_f32 && rel_extent % 8 == 0 && aligned(rel_logits->data, 16)) ? 1 : 0;
     p.out = out->data;
     p.o_st = out->stride[0];
     p.o_sh = out->stride[1];

@@ -68,6 +68,13 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// rel_logits element idx of a bf16 or fp32 tensor, as fp32 (read-only path).
+__device__ __forceinline__ float rel_at(const void* rel, bool f32, size_t idx) {
+    if (f32) return __ldg(static_cast<const float*>(rel) + idx);
+    const uint16_t b = __ldg(static_cast<const uint16_t*>(rel) + idx);
+    return __uint_as_float(((uint32_t)b) << 16);
+}
+
 // n arrivals in one operation.
 __device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t n) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(n) : "memory");

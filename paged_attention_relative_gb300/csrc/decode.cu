@@ -23,6 +23,8 @@
 
 #include <math_constants.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -52,7 +54,11 @@ struct DecodeCfg {
 
 constexpr int kRankMax = 256;
 
-template <int D, int MT, int KSL>
+__device__ __forceinline__ float bias_to_f32(uint16_t b) { return bf16_bits_to_f32(b); }
+__device__ __forceinline__ float bias_to_f32(float b) { return b; }
+
+// BF32: rel_logits are fp32 (else bf16).
+template <int D, int MT, int KSL, bool BF32>
 __global__ void __launch_bounds__(DecodeCfg<D, MT, KSL>::kMaxThreads) decode_kernel(const AttnParams p) {
     using C = DecodeCfg<D, MT, KSL>;
     extern __shared__ uint8_t smem_raw[];
@@ -185,11 +191,13 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, KSL>::kMaxThreads) decode_ker
     const int qi0 = valid0 ? r0 / G : 0, qi1 = valid1 ? r1 / G : 0;
     const int pos0 = qi0 + off, pos1 = qi1 + off;  // key positions of the two rows
     const int h0 = g * G + (valid0 ? r0 % G : 0), h1 = g * G + (valid1 ? r1 % G : 0);
-    const uint16_t* rel0 = nullptr;
-    const uint16_t* rel1 = nullptr;
+    // The two rows' rel_logits (bf16 bits or fp32 values).
+    using BiasT = typename std::conditional<BF32, float, uint16_t>::type;
+    const BiasT* rel0 = nullptr;
+    const BiasT* rel1 = nullptr;
     if (p.R > 0) {
-        rel0 = reinterpret_cast<const uint16_t*>(p.rel) + ((size_t)(q0 + qi0) * p.H + h0) * p.R;
-        rel1 = reinterpret_cast<const uint16_t*>(p.rel) + ((size_t)(q0 + qi1) * p.H + h1) * p.R;
+        rel0 = reinterpret_cast<const BiasT*>(p.rel) + ((size_t)(q0 + qi0) * p.H + h0) * p.R;
+        rel1 = reinterpret_cast<const BiasT*>(p.rel) + ((size_t)(q0 + qi1) * p.H + h1) * p.R;
     }
     // Extreme key positions over the CTA's valid rows (rows are token-major).
     const int pos_lo = off, pos_hi = (n_rows - 1) / G + off;
@@ -280,7 +288,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, KSL>::kMaxThreads) decode_ker
                 for (int e = 0; e < 4; ++e) {
                     const bool second = e >> 1;
                     const int pos = second ? pos1 : pos0;
-                    const uint16_t* relr = second ? rel1 : rel0;
+                    const BiasT* relr = second ? rel1 : rel0;
                     const int j = jb + nt * 8 + 2 * tig + (e & 1);
                     const int d = pos - j;
                     bool allowed = (second ? valid1 : valid0) && j < khi;
@@ -288,7 +296,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, KSL>::kMaxThreads) decode_ker
                     if (wl >= 0) allowed = allowed && d <= wl;
                     if (wr >= 0) allowed = allowed && d >= -wr;
                     float bias = 0.f;
-                    if (allowed && d >= 0 && d < R) bias = bf16_bits_to_f32(__ldg(relr + d));
+                    if (allowed && d >= 0 && d < R) bias = bias_to_f32(__ldg(relr + d));
                     s[nt][e] = allowed ? fmaf(sacc[nt][e] + sacc2[nt][e], sl2, bias * kLog2e) : -CUDART_INF_F;
                 }
             }
@@ -458,9 +466,9 @@ int pick_stages(int ctas, int num_sms) {
     return n;
 }
 
-template <int D, int MT, int KSL>
+template <int D, int MT, int KSL, bool BF32>
 cudaError_t launch_t(const AttnParams& p, const LaunchShape& s, cudaStream_t stream) {
-    auto kern = decode_kernel<D, MT, KSL>;
+    auto kern = decode_kernel<D, MT, KSL, BF32>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, s.smem);
     if (e != cudaSuccess) return e;
     kern<<<s.grid, s.block, s.smem, stream>>>(p);
@@ -470,8 +478,7 @@ cudaError_t launch_t(const AttnParams& p, const LaunchShape& s, cudaStream_t str
 }  // namespace
 
 // Tile shape: up to 16 packed rows use one 16-row MMA tile and 8 key groups
-// (8 warps) when the grid fits in one wave, else 4 groups so that two CTAs
-// share an SM; 17-32 rows use 2 row tiles x 4 groups, 33-64 rows 4 x 2.
+// (8 warps); 17-32 rows use 2 row tiles x 4 groups, 33-64 rows 4 x 2.
 LaunchShape decode_shape(const AttnParams& p, int num_sms) {
     LaunchShape s;
     const int ctas = p.num_splits * p.Hk * p.B;
@@ -499,11 +506,9 @@ LaunchShape decode_shape(const AttnParams& p, int num_sms) {
         s.nstage = pick_stages<DD, M, K>(ctas, num_sms); \
         s.smem = decode_smem_bytes<DD, M, K>(s.nstage); \
     }
-    REL_ATTN_SHAPE(64, 1, 4)
     REL_ATTN_SHAPE(64, 1, 8)
     REL_ATTN_SHAPE(64, 2, 4)
     REL_ATTN_SHAPE(64, 4, 2)
-    REL_ATTN_SHAPE(128, 1, 4)
     REL_ATTN_SHAPE(128, 1, 8)
     REL_ATTN_SHAPE(128, 2, 4)
     REL_ATTN_SHAPE(128, 4, 2)
@@ -512,13 +517,12 @@ LaunchShape decode_shape(const AttnParams& p, int num_sms) {
 }
 
 cudaError_t launch_decode(const AttnParams& p, const LaunchShape& s, cudaStream_t stream) {
-#define REL_ATTN_LAUNCH(DD, M, K) \
-    if (p.D == DD && s.mt == M && s.ksl == K) return launch_t<DD, M, K>(p, s, stream);
-    REL_ATTN_LAUNCH(64, 1, 4)
+#define REL_ATTN_LAUNCH(DD, M, K)                                                                      \
+    if (p.D == DD && s.mt == M && s.ksl == K)                                                          \
+        return p.bias_f32 ? launch_t<DD, M, K, true>(p, s, stream) : launch_t<DD, M, K, false>(p, s, stream);
     REL_ATTN_LAUNCH(64, 1, 8)
     REL_ATTN_LAUNCH(64, 2, 4)
     REL_ATTN_LAUNCH(64, 4, 2)
-    REL_ATTN_LAUNCH(128, 1, 4)
     REL_ATTN_LAUNCH(128, 1, 8)
     REL_ATTN_LAUNCH(128, 2, 4)
     REL_ATTN_LAUNCH(128, 4, 2)

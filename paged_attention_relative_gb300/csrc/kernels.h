@@ -20,8 +20,9 @@ struct AttnParams {
     int32_t max_blocks;        // MB
     const int32_t* cache_seqlens;
     const int32_t* cu_seqlens_q;
-    const void* rel;           // (T, H, R) bf16 contiguous, or null when R == 0
+    const void* rel;           // (T, H, R) bf16 (or fp32 when bias_f32) contiguous, or null when R == 0
     int32_t R;
+    int32_t bias_f32;          // rel_logits are fp32
     void* out;                 // (T, H, D) bf16, or fp32 when out_f32
     int64_t o_st, o_sh;
     int32_t out_f32;

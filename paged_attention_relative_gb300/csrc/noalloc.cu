@@ -117,10 +117,10 @@ extern "C" rel_attn_status rel_attn_paged_varlen_noalloc(
     if (num_splits < 1 || rel_extent < 0 || max_seqlen_q < 0)
         return nfail(bad, "noalloc: num_splits >= 1, rel_extent >= 0 and max_seqlen_q >= 0 are required");
     if (rel_extent > 0 &&
-        (!is(rel_logits, REL_ATTN_BF16, 3) || rel_logits->shape[0] != T || rel_logits->shape[1] != H ||
+        (!(is(rel_logits, REL_ATTN_BF16, 3) || is(rel_logits, REL_ATTN_F32, 3)) || rel_logits->shape[0] != T || rel_logits->shape[1] != H ||
          rel_logits->shape[2] != rel_extent || rel_logits->stride[2] != 1 || rel_logits->stride[1] != rel_extent ||
          rel_logits->stride[0] != H * rel_extent))
-        return nfail(bad, "noalloc: rel_logits must be a contiguous (T, H, rel_extent) bf16 tensor");
+        return nfail(bad, "noalloc: rel_logits must be a contiguous (T, H, rel_extent) bf16 or fp32 tensor");
     if (q->stride[2] != 1 || out->stride[2] != 1 || key_cache->stride[3] != 1)
         return nfail(bad, "noalloc: the head_dim axis must be contiguous");
     if (D != 64 && D != 128) return nfail(REL_ATTN_ERR_UNSUPPORTED, "noalloc: head_dim must be 64 or 128");
@@ -176,6 +176,7 @@ extern "C" rel_attn_status rel_attn_paged_varlen_noalloc(
     p.cache_seqlens = static_cast<const int32_t*>(cache_seqlens->data);
     p.cu_seqlens_q = static_cast<const int32_t*>(cu_seqlens_q->data);
     p.rel = rel_extent > 0 ? rel_logits->data : nullptr;
+    p.bias_f32 = rel_extent > 0 && rel_logits->dtype == REL_ATTN_F32 ? 1 : 0;
     p.R = rel_extent;
     p.out = out->data;
     p.o_st = out->stride[0];

@@ -543,7 +543,7 @@ __global__ void __launch_bounds__(384, 1)
         if (p.wr >= 0) khi = min(khi, pos + p.wr + 1);
         int klo = 0;
         if (p.wl >= 0) klo = max(0, pos - p.wl);
-        const uint16_t* relg = reinterpret_cast<const uint16_t*>(p.rel);
+        const bool bias_f32 = p.bias_f32 != 0;
         const size_t rel_row = ((size_t)t * p.H + h) * (size_t)R;
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const float sc = p.scale;          // scores are kept in natural units: sc * q.k + bias
@@ -646,11 +646,9 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                             for (int e = 0; e < 32; ++e) {
                                 const int d = pos - (jh + 2 * e);
-                                const float b0 =
-                                    valid && d >= 0 && d < R ? bf16_bits_to_f32(__ldg(relg + rel_row + d)) : 0.f;
-                                const float b1 = valid && d - 1 >= 0 && d - 1 < R
-                                                     ? bf16_bits_to_f32(__ldg(relg + rel_row + d - 1))
-                                                     : 0.f;
+                                const float b0 = valid && d >= 0 && d < R ? rel_at(p.rel, bias_f32, rel_row + d) : 0.f;
+                                const float b1 =
+                                    valid && d - 1 >= 0 && d - 1 < R ? rel_at(p.rel, bias_f32, rel_row + d - 1) : 0.f;
                                 s[e] = __ffma2_rn(s[e], sc2, make_float2(b0, b1));
                             }
                         }

@@ -374,3 +374,20 @@ def test_append_then_attend_equals_sdpa_over_prefix_and_new_rows():
         want = F.scaled_dot_product_attention(q, k, v, attn_mask=causal_lower_right(sq, sk),
                                               scale=float(np.float32(c.softmax_scale)))
         np.testing.assert_allclose(out[cu[b]:cu[b + 1]], want.transpose(0, 1).numpy(), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("i", [0, 2, 8])
+def test_fp32_rel_logits_c_oracle_equals_brute_force(i):
+    """fp32 rel_logits (values bf16 cannot hold) take the same definition."""
+    c = _small(100 + i, **BRUTE_CASES[i])
+    g = torch.Generator().manual_seed(i)
+    rel = c.rel_logits.float() + 1e-3 * torch.randn(c.rel_logits.shape, generator=g)
+    c = c.with_(rel_logits=rel)
+    out, lse = ref.forward(c, with_lse=True)
+    want, want_lse = ref.brute_force(c, with_lse=True)
+    np.testing.assert_allclose(out, want, rtol=0, atol=1e-12)
+    fin = np.isfinite(want_lse)
+    np.testing.assert_allclose(lse[fin], want_lse[fin], rtol=0, atol=1e-12)
+    # and the fp32 values are used as they are, not rounded to bf16
+    c16 = c.with_(rel_logits=rel.to(torch.bfloat16))
+    assert np.abs(ref.forward(c16) - out).max() > 1e-6
