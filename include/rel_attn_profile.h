@@ -52,6 +52,20 @@ rel_attn_status rel_attn_set_kernel_events(void* begin, void* end);
  */
 rel_attn_status rel_attn_device_error(int32_t* code);
 
+/* Wait-site code that rel_attn_check_wait_timeout records. */
+#define REL_ATTN_SITE_SELF_TEST 99
+
+/*
+ * Self-test of the bounded-wait path: launch on `stream` a one-thread kernel
+ * whose single mbarrier wait is never satisfied; after timeout_ms (1..10000)
+ * it records REL_ATTN_SITE_SELF_TEST in the device error word (unless a code
+ * is already there) and returns, as the attention kernels do when a hand-off
+ * never comes.  The device stays usable; read the word with
+ * rel_attn_device_error.  Returns INVALID_ARGUMENT for a timeout outside the
+ * range, CUDA for a launch error.
+ */
+rel_attn_status rel_attn_check_wait_timeout(int32_t timeout_ms, rel_attn_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -11,7 +11,7 @@ from __future__ import annotations
 def __getattr__(name):
     if name in ("rel_attn_paged_varlen", "rel_attn_paged_varlen_lse", "rel_attn_paged_varlen_noalloc", "rel_attn_cache_append", "rel_attn_num_splits",
                 "rel_attn_bucket_max_seqlen_q", "last_launch", "set_kernel_events", "device_error", "RelAttnError",
-                "describe"):
+                "describe", "check_wait_timeout", "SITE_SELF_TEST"):
         from . import _lib
         return getattr(_lib, name)
     raise AttributeError(name)

@@ -24,7 +24,8 @@ KERNELS = {0: "none", 1: "decode", 2: "prefill", 3: "append"}
 EXPORTS = ("rel_attn_paged_varlen", "rel_attn_paged_varlen_lse", "rel_attn_paged_varlen_noalloc", "rel_attn_num_splits",
            "rel_attn_cache_append",
            "rel_attn_bucket_max_seqlen_q",
-           "rel_attn_last_error", "rel_attn_last_launch", "rel_attn_set_kernel_events", "rel_attn_device_error")
+           "rel_attn_last_error", "rel_attn_last_launch", "rel_attn_set_kernel_events", "rel_attn_device_error",
+           "rel_attn_check_wait_timeout")
 
 
 class RelAttnTensor(ctypes.Structure):
@@ -72,6 +73,8 @@ def _load() -> ctypes.CDLL:
     lib.rel_attn_set_kernel_events.restype = ctypes.c_int
     lib.rel_attn_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32)]
     lib.rel_attn_device_error.restype = ctypes.c_int
+    lib.rel_attn_check_wait_timeout.argtypes = [i32, ctypes.c_void_p]
+    lib.rel_attn_check_wait_timeout.restype = ctypes.c_int
     return lib
 
 
@@ -227,3 +230,13 @@ def device_error() -> int:
     code = ctypes.c_int32(0)
     _check(lib.rel_attn_device_error(ctypes.byref(code)))
     return code.value
+
+
+SITE_SELF_TEST = 99  # REL_ATTN_SITE_SELF_TEST
+
+
+def check_wait_timeout(timeout_ms: int, stream=None):
+    """Launch the bounded-wait self-test (include/rel_attn_profile.h)."""
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    _check(lib.rel_attn_check_wait_timeout(int(timeout_ms), ctypes.c_void_p(stream)))

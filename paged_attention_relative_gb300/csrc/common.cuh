@@ -25,6 +25,7 @@ enum WaitSite : int {
     kSitePrefillRelEmpty = 19,
     kSitePrefillSEmpty = 20,
     kSitePrefillXchg = 21,
+    kSiteSelfTest = 99,  // rel_attn_check_wait_timeout
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -199,3 +199,9 @@ def test_cache_append_validates_before_device_work(what):
         L.rel_attn_cache_append(key, value, c.key_cache, c.value_cache, c.block_table, c.cache_seqlens,
                                 c.cu_seqlens_q, stream=0)
     assert ei.value.status == 1
+
+
+@pytest.mark.parametrize("ms", [0, -5, 10001])
+def test_wait_timeout_self_test_rejects_out_of_range_limits(ms):
+    L = _lib()
+    assert L.lib.rel_attn_check_wait_timeout(ms, None) == 1
