@@ -174,3 +174,39 @@ def test_single_key_returns_v():
         v0 = c.value_cache[int(c.block_table[b, 0]), 0]
         for h in range(4):
             assert torch.equal(got[b, h], v0[h // 2].float())
+
+
+@pytest.mark.parametrize("splits", [1, 2])
+def test_decode_more_requests_than_the_ranked_limit(splits):
+    """700 requests (above the 256 the kernel ranks by length): CTAs take
+    requests in index order; lengths include empty caches."""
+    import numpy as np
+    import paged_attention_relative_gb300 as pa
+    rng = np.random.default_rng(17)
+    sk = rng.integers(0, 400, size=700)
+    c = make_case(seed=18, seqlens_q=[1] * 700, seqlens_k=sk.tolist(), num_heads=16, num_kv_heads=2,
+                  head_dim=64, rel_extent=24)
+    got = run(c, num_splits=splits)
+    assert pa.last_launch()["kernel"] == "decode"
+    assert_close(got, ref.forward(c), what=f"700 requests splits={splits}")
+    assert_no_device_error()
+
+
+@pytest.mark.parametrize("sq,kernel", [(16, "decode"), (17, "prefill")])
+def test_kernel_boundary_at_64_packed_rows(sq, kernel):
+    """64 GQA-packed rows (16 tokens x 4 heads) is the decode kernel's
+    largest case; 65 and above go to the tensor-core prefill kernel."""
+    import paged_attention_relative_gb300 as pa
+    c = make_case(seed=19, seqlens_q=[sq, 3], seqlens_k=[500, 90], num_heads=8, num_kv_heads=2, head_dim=128,
+                  rel_extent=40)
+    got = run(c)
+    assert pa.last_launch()["kernel"] == kernel
+    assert_close(got, ref.forward(c), what=f"sq={sq}")
+
+
+@pytest.mark.parametrize("sq", [[1, 2], [70, 20]], ids=["decode", "prefill"])
+def test_block_size_64(sq):
+    c = make_case(seed=20, seqlens_q=sq, seqlens_k=[333, 129], num_heads=8, num_kv_heads=2, head_dim=128,
+                  rel_extent=32, block_size=64)
+    assert_close(run(c, num_splits=2), ref.forward(c), what=f"block 64 {sq}")
+    assert_no_device_error()
