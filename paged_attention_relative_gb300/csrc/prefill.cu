@@ -66,6 +66,8 @@
 
 #include <math_constants.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -501,25 +503,42 @@ __global__ void __launch_bounds__(384, 1)
                 umma_commit(&bars->o_done);
                 umma_commit_mc(&bars->kv_empty[slot], mc_mask);
             };
-            for (int jj = 0; jj < n_it && ok; ++jj) {
-                const int sb = jj & 1;
-                const int slot = jj % C::kKRing;
-                const uint64_t dk = dK0 + (uint64_t)((slot * C::kTileBytes) >> 4);
+            // Tile jj's S buffer, K slot and V slot depend on jj % 2 only when
+            // both rings have two slots: unroll by two so every descriptor and
+            // TMEM address is a constant.
+            auto issue_s = [&](int jj, auto par) {
+                constexpr int P = decltype(par)::value;
+                constexpr int slot = C::kKRing == 2 ? P : 0;
+                const int slot_rt = C::kKRing == 2 ? P : jj % C::kKRing;
+                const uint64_t dk = dK0 + (uint64_t)((slot_rt * C::kTileBytes) >> 4);
                 uint64_t dK[D / 16];
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) dK[kk] = dk + (uint64_t)((((kk >> 2) * C::kBlk) + (kk & 3) * 32) >> 4);
-                const uint32_t sd = tmem + sb * C::BN;
-                ok = ok && mbar_wait(&bars->kv_full[slot], (jj / C::kKRing) & 1, p.timeout_ns, kSitePrefillKFull,
+                const uint32_t sd = tmem + P * C::BN;
+                (void)slot;
+                ok = ok && mbar_wait(&bars->kv_full[slot_rt], (jj / C::kKRing) & 1, p.timeout_ns, kSitePrefillKFull,
                                      p.err);
-                if (!ok) break;
+                if (!ok) return;
                 tc_fence_after();
                 umma_ts<0>(sd, aq, dK[0], idS);
 #pragma unroll
                 for (int kk = 1; kk < D / 16; ++kk) umma_ts<1>(sd, aq + 8 * kk, dK[kk], idS);
-                umma_commit(&bars->s_full[sb]);
-                umma_commit_mc(&bars->kv_empty[slot], mc_mask);
+                umma_commit(&bars->s_full[P]);
+                umma_commit_mc(&bars->kv_empty[slot_rt], mc_mask);
+            };
+            using I0 = std::integral_constant<int, 0>;
+            using I1 = std::integral_constant<int, 1>;
+            for (int jj = 0; jj < n_it && ok; jj += 2) {
+                issue_s(jj, I0{});
+                if (!ok) break;
                 if (jj >= 1) issue_pv(jj - 1);
+                if (jj + 1 < n_it) {
+                    issue_s(jj + 1, I1{});
+                    if (!ok) break;
+                    issue_pv(jj);
+                }
             }
+            // The last tile's PV follows.
             if (ok) issue_pv(n_it - 1);
             // The epilogue may be two or more o_done phases behind, where a
             // parity wait cannot tell phases apart: give it its own barrier.
