@@ -337,13 +337,17 @@ def run_append(args, rank, world):
     for _ in range(max(args.warmup, 3)):
         call(kd, vd)
     torch.cuda.synchronize()
+    # Events recorded by the library right around the launch (no host work inside).
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for b, e in evs:          # torch creates the CUDA event on first record
+        b.record(stream)
+        e.record(stream)
     with ClockSampler(dev.index) as clocks:
         for b, e in evs:
             flush.sum()
-            b.record(stream)
+            pa.set_kernel_events(b, e)
             call(kd, vd)
-            e.record(stream)
+        pa.set_kernel_events(None, None)
         torch.cuda.synchronize()
     kern_ms = max_over_ranks(sum(b.elapsed_time(e) for b, e in evs) / args.steps, world, dev)
     rows = 2 * d["T"] * d["Hk"] * d["D"] * 2

@@ -37,9 +37,9 @@ typedef struct {
 rel_attn_status rel_attn_last_launch(rel_attn_launch_info* info);
 
 /*
- * Record `begin` just before and `end` just after the main attention kernel
- * of every following rel_attn_paged_varlen call on this thread, on that call's
- * stream.  Both are cudaEvent_t handles owned by the caller; pass NULL, NULL
+ * Record `begin` just before and `end` just after the main kernel of every
+ * following rel_attn_paged_varlen, rel_attn_paged_varlen_lse or
+ * rel_attn_cache_append call on this thread, on that call's stream.  Both are cudaEvent_t handles owned by the caller; pass NULL, NULL
  * to stop.  Lets a benchmark time the dominant kernel alone with CUDA events.
  */
 rel_attn_status rel_attn_set_kernel_events(void* begin, void* end);
