@@ -19,6 +19,8 @@ CASES = [
          head_dim=64),
     dict(name="block32", seqlens_q=[33, 1], seqlens_k=[70, 32], num_heads=8, num_kv_heads=8, head_dim=128,
          block_size=32),
+    # a request with new tokens but an empty cache writes nothing
+    dict(name="empty_cache", seqlens_q=[3, 4], seqlens_k=[0, 10], num_heads=4, num_kv_heads=2, head_dim=128),
 ]
 
 

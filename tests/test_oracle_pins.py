@@ -342,15 +342,18 @@ def test_cache_append_round_trip_through_block_table():
 
 
 def test_cache_append_skips_tokens_without_a_slot():
-    """sk < sq: the first sq - sk tokens have negative positions and write nothing."""
-    c = _small(41, seqlens_q=[5], seqlens_k=[2])
+    """sk < sq: the first sq - sk tokens have negative positions and write
+    nothing; a request with an empty cache writes nothing at all (which tells
+    skipping apart from clamping the position to 0)."""
+    c = _small(41, seqlens_q=[5, 3], seqlens_k=[2, 0])
     key, value = _new_rows(c, 2)
-    kc, _ = ref.cache_append(c, key, value)
+    kc, vc = ref.cache_append(c, key, value)
     got = _kv_contig(c.with_(key_cache=kc), 0, "k")
     assert torch.equal(got, key[3:5].double())
     untouched = torch.ones(kc.shape[:2], dtype=torch.bool)
     untouched[int(c.block_table[0, 0]), 0:2] = False
     assert torch.equal(kc[untouched], c.key_cache[untouched])
+    assert torch.equal(vc[untouched], c.value_cache[untouched])
 
 
 def test_append_then_attend_equals_sdpa_over_prefix_and_new_rows():
