@@ -497,8 +497,8 @@ LaunchShape decode_shape(const AttnParams& p, int num_sms) {
         s.ksl = 2;
     }
     s.grid = dim3(p.num_splits, p.Hk, p.B);
-    // Two producer warps per CTA, four when one CTA owns the SM: a single
-    // issuing warp cannot keep enough 16-byte gathers in flight.
+    // Four producer warps next to the eight consumers: a single issuing warp
+    // cannot keep enough 16-byte gathers in flight.
     s.nprod = s.mt * s.ksl >= 8 ? 4 : 2;
     s.block = (s.mt * s.ksl + s.nprod) * 32;
 #define REL_ATTN_SHAPE(DD, M, K)                         \
