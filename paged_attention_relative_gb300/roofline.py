@@ -33,7 +33,8 @@ def algorithmic_bytes(case: Case) -> int:
         rel_elems += _rel_band_elems(sq[b], sk[b], case.causal, wl, wr, case.rel_extent)
     kv = kv_rows * d["Hk"] * d["D"] * 2 * 2
     qo = 2 * d["T"] * d["H"] * d["D"] * 2
-    rel = rel_elems * d["H"] * 2
+    rel_bytes = case.rel_logits.element_size() if case.rel_extent > 0 else 2  # bf16 or fp32
+    rel = rel_elems * d["H"] * rel_bytes
     meta = case.block_table.numel() * 4 + case.cache_seqlens.numel() * 4 + case.cu_seqlens_q.numel() * 4
     return int(kv + qo + rel + meta)
 
