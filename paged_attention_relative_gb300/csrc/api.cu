@@ -202,6 +202,31 @@ __global__ void check_kernel(const int32_t* cu, const int32_t* seqk, const int32
     if (code) atomicCAS(err, 0, code);
 }
 
+
+// REL_ATTN_CHECK=1: run check_kernel on `stream`, wait for it, and turn a
+// recorded violation into REL_ATTN_ERR_DEVICE_CHECK (no kernel runs after it).
+rel_attn_status run_device_check(DeviceInfo* dev, cudaStream_t stream, const rel_attn_tensor* cu_seqlens_q,
+                                 const rel_attn_tensor* cache_seqlens, const rel_attn_tensor* block_table,
+                                 int64_t B, int64_t T, int64_t MB, int64_t BS, int64_t NB, int max_seqlen_q) {
+    cudaError_t e = cudaMemsetAsync(dev->check_err, 0, sizeof(int), stream);
+    if (e == cudaSuccess) {
+        check_kernel<<<(unsigned)((B + 127) / 128), 128, 0, stream>>>(
+            static_cast<const int32_t*>(cu_seqlens_q->data), static_cast<const int32_t*>(cache_seqlens->data),
+            static_cast<const int32_t*>(block_table->data), block_table->stride[0], (int)B, (int)T, (int)MB,
+            (int)BS, (int)NB, max_seqlen_q, dev->check_err);
+        e = cudaGetLastError();
+    }
+    int code = 0;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&code, dev->check_err, sizeof code, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return fail(REL_ATTN_ERR_CUDA, "check kernel: %s", cudaGetErrorString(e));
+    if (code)
+        return fail(REL_ATTN_ERR_DEVICE_CHECK, "device-side precondition violated (code %d: %s)", code,
+                    code == 1 ? "cu_seqlens_q[0] != 0" : code == 2 ? "cu_seqlens_q[B] != T"
+                    : code == 3 ? "cu_seqlens_q decreasing" : code == 4 ? "a query length exceeds max_seqlen_q"
+                    : code == 5 ? "cache_seqlens outside [0, MB*BS]" : "block id outside [0, NB)");
+    return REL_ATTN_OK;
+}
 }  // namespace
 }  // namespace relattn
 
@@ -386,25 +411,9 @@ rel_attn_status paged_varlen(
     const int64_t rows = (int64_t)max_seqlen_q * G;
     const bool prefill = rows > 64;  // decode kernel up to 64 packed rows, tcgen05 tiles above
 
-    if (check_enabled()) {
-        cudaError_t e = cudaMemsetAsync(dev->check_err, 0, sizeof(int), stream);
-        if (e == cudaSuccess) {
-            check_kernel<<<(unsigned)((B + 127) / 128), 128, 0, stream>>>(
-                static_cast<const int32_t*>(cu_seqlens_q->data), static_cast<const int32_t*>(cache_seqlens->data),
-                static_cast<const int32_t*>(block_table->data), block_table->stride[0], (int)B, (int)T, (int)MB,
-                (int)BS, (int)NB, max_seqlen_q, dev->check_err);
-            e = cudaGetLastError();
-        }
-        int code = 0;
-        if (e == cudaSuccess) e = cudaMemcpyAsync(&code, dev->check_err, sizeof code, cudaMemcpyDeviceToHost, stream);
-        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
-        if (e != cudaSuccess) return fail(REL_ATTN_ERR_CUDA, "check kernel: %s", cudaGetErrorString(e));
-        if (code)
-            return fail(REL_ATTN_ERR_DEVICE_CHECK, "device-side precondition violated (code %d: %s)", code,
-                        code == 1 ? "cu_seqlens_q[0] != 0" : code == 2 ? "cu_seqlens_q[B] != T"
-                        : code == 3 ? "cu_seqlens_q decreasing" : code == 4 ? "a query length exceeds max_seqlen_q"
-                        : code == 5 ? "cache_seqlens outside [0, MB*BS]" : "block id outside [0, NB)");
-    }
+    if (check_enabled() && (st = run_device_check(dev, stream, cu_seqlens_q, cache_seqlens, block_table, B, T, MB,
+                                                   BS, NB, max_seqlen_q)))
+        return st;
 
     AttnParams p{};
     p.q = q->data;
@@ -613,21 +622,9 @@ extern "C" rel_attn_status rel_attn_cache_append(
     if ((st = device_info(&dev))) return st;
     if (dev->major != 10 || dev->minor != 3)
         return fail(REL_ATTN_ERR_UNSUPPORTED, "built for sm_103a; device is sm_%d%d", dev->major, dev->minor);
-    if (check_enabled()) {
-        cudaError_t e = cudaMemsetAsync(dev->check_err, 0, sizeof(int), stream);
-        if (e == cudaSuccess) {
-            check_kernel<<<(unsigned)((B + 127) / 128), 128, 0, stream>>>(
-                static_cast<const int32_t*>(cu_seqlens_q->data), static_cast<const int32_t*>(cache_seqlens->data),
-                static_cast<const int32_t*>(block_table->data), block_table->stride[0], (int)B, (int)T, (int)MB,
-                (int)BS, (int)NB, (int)T, dev->check_err);
-            e = cudaGetLastError();
-        }
-        int code = 0;
-        if (e == cudaSuccess) e = cudaMemcpyAsync(&code, dev->check_err, sizeof code, cudaMemcpyDeviceToHost, stream);
-        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
-        if (e != cudaSuccess) return fail(REL_ATTN_ERR_CUDA, "check kernel: %s", cudaGetErrorString(e));
-        if (code) return fail(REL_ATTN_ERR_DEVICE_CHECK, "device-side precondition violated (code %d)", code);
-    }
+    if (check_enabled() && (st = run_device_check(dev, stream, cu_seqlens_q, cache_seqlens, block_table, B, T, MB,
+                                                   BS, NB, (int)T)))
+        return st;
     AppendParams p{};
     p.key = key->data;
     p.value = value->data;
