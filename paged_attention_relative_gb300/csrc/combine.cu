@@ -20,6 +20,9 @@ namespace {
 template <int D>
 __global__ void __launch_bounds__(256) combine_kernel(const AttnParams p) {
     constexpr int V = D / 32;
+    // Launched as a programmatic dependent of the attention kernel: start up
+    // while it finishes, read its partials only once it has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long rows = (long long)p.T * p.H;
     const long long row = (long long)blockIdx.x * 8 + warp;
@@ -109,13 +112,24 @@ __global__ void __launch_bounds__(256) combine_kernel(const AttnParams p) {
 
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t stream) {
     const long long rows = (long long)p.T * p.H;
-    const unsigned blocks = (unsigned)((rows + 7) / 8);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((rows + 7) / 8));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
     if (p.D == 128)
-        combine_kernel<128><<<blocks, 256, 0, stream>>>(p);
+        e = cudaLaunchKernelEx(&cfg, combine_kernel<128>, p);
     else if (p.D == 64)
-        combine_kernel<64><<<blocks, 256, 0, stream>>>(p);
+        e = cudaLaunchKernelEx(&cfg, combine_kernel<64>, p);
     else
         return cudaErrorInvalidValue;
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
