@@ -108,6 +108,25 @@ def _check(status: int):
         raise RelAttnError(status, lib.rel_attn_last_error().decode())
 
 
+def _stream_handle(stream, device):
+    """A cudaStream_t as an int: torch's current stream when None."""
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return stream
+
+
+def _attn_args(q, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_q, max_seqlen_q, softmax_scale,
+               causal, window_left, window_right, rel_extent, rel_logits, num_splits):
+    """The leading arguments shared by the three attention entry points (the
+    byref objects keep their descriptors alive for the call)."""
+    descs = [describe(t) for t in (q, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_q)]
+    rel = describe(rel_logits) if rel_extent > 0 else None
+    return [*[_ref(d) for d in descs], int(max_seqlen_q), float(softmax_scale), int(bool(causal)),
+            int(window_left), int(window_right), int(rel_extent), _ref(rel), int(num_splits)]
+
+
 def rel_attn_paged_varlen(q, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_q, max_seqlen_q,
                           softmax_scale, causal, window_left, window_right, rel_extent, rel_logits, num_splits,
                           out=None, stream=None):
@@ -118,17 +137,10 @@ def rel_attn_paged_varlen(q, key_cache, value_cache, block_table, cache_seqlens,
     """
     if out is None:
         out = torch.empty_like(q)
-    if stream is None:
-        stream = torch.cuda.current_stream(q.device).cuda_stream
-    elif isinstance(stream, torch.cuda.Stream):
-        stream = stream.cuda_stream
-    descs = [describe(t) for t in (q, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_q)]
-    rel = describe(rel_logits) if rel_extent > 0 else None
+    args = _attn_args(q, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_q, max_seqlen_q,
+                      softmax_scale, causal, window_left, window_right, rel_extent, rel_logits, num_splits)
     od = describe(out)
-    st = lib.rel_attn_paged_varlen(*[_ref(d) for d in descs], int(max_seqlen_q), float(softmax_scale),
-                                   int(bool(causal)), int(window_left), int(window_right), int(rel_extent),
-                                   _ref(rel), int(num_splits), _ref(od), ctypes.c_void_p(stream))
-    _check(st)
+    _check(lib.rel_attn_paged_varlen(*args, _ref(od), ctypes.c_void_p(_stream_handle(stream, q.device))))
     return out
 
 
@@ -145,18 +157,11 @@ def rel_attn_paged_varlen_lse(q, key_cache, value_cache, block_table, cache_seql
         out = torch.empty_like(q)
     if softmax_lse is None:
         softmax_lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
-    if stream is None:
-        stream = torch.cuda.current_stream(q.device).cuda_stream
-    elif isinstance(stream, torch.cuda.Stream):
-        stream = stream.cuda_stream
-    descs = [describe(t) for t in (q, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_q)]
-    rel = describe(rel_logits) if rel_extent > 0 else None
-    od = describe(out)
-    ld = describe(softmax_lse)
-    st = lib.rel_attn_paged_varlen_lse(*[_ref(d) for d in descs], int(max_seqlen_q), float(softmax_scale),
-                                       int(bool(causal)), int(window_left), int(window_right), int(rel_extent),
-                                       _ref(rel), int(num_splits), _ref(od), _ref(ld), ctypes.c_void_p(stream))
-    _check(st)
+    args = _attn_args(q, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_q, max_seqlen_q,
+                      softmax_scale, causal, window_left, window_right, rel_extent, rel_logits, num_splits)
+    od, ld = describe(out), describe(softmax_lse)
+    _check(lib.rel_attn_paged_varlen_lse(*args, _ref(od), _ref(ld),
+                                         ctypes.c_void_p(_stream_handle(stream, q.device))))
     return out, softmax_lse
 
 
@@ -164,30 +169,18 @@ def rel_attn_paged_varlen_noalloc(q, key_cache, value_cache, block_table, cache_
                                   max_seqlen_q, softmax_scale, causal, window_left, window_right, rel_extent,
                                   rel_logits, num_splits, out, stream=None):
     """The allocation-free decode entry point; ``out`` must be provided."""
-    if stream is None:
-        stream = torch.cuda.current_stream(q.device).cuda_stream
-    elif isinstance(stream, torch.cuda.Stream):
-        stream = stream.cuda_stream
-    descs = [describe(t) for t in (q, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_q)]
-    rel = describe(rel_logits) if rel_extent > 0 else None
+    args = _attn_args(q, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_q, max_seqlen_q,
+                      softmax_scale, causal, window_left, window_right, rel_extent, rel_logits, num_splits)
     od = describe(out)
-    st = lib.rel_attn_paged_varlen_noalloc(*[_ref(d) for d in descs], int(max_seqlen_q), float(softmax_scale),
-                                           int(bool(causal)), int(window_left), int(window_right),
-                                           int(rel_extent), _ref(rel), int(num_splits), _ref(od),
-                                           ctypes.c_void_p(stream))
-    _check(st)
+    _check(lib.rel_attn_paged_varlen_noalloc(*args, _ref(od), ctypes.c_void_p(_stream_handle(stream, q.device))))
     return out
 
 
 def rel_attn_cache_append(key, value, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_q,
                           stream=None):
     """Write the new tokens' key/value rows into the paged caches; see include/rel_attn.h."""
-    if stream is None:
-        stream = torch.cuda.current_stream(key.device).cuda_stream
-    elif isinstance(stream, torch.cuda.Stream):
-        stream = stream.cuda_stream
     d = [describe(t) for t in (key, value, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_q)]
-    _check(lib.rel_attn_cache_append(*[_ref(x) for x in d], ctypes.c_void_p(stream)))
+    _check(lib.rel_attn_cache_append(*[_ref(x) for x in d], ctypes.c_void_p(_stream_handle(stream, key.device))))
     return key_cache, value_cache
 
 
@@ -237,6 +230,4 @@ SITE_SELF_TEST = 99  # REL_ATTN_SITE_SELF_TEST
 
 def check_wait_timeout(timeout_ms: int, stream=None):
     """Launch the bounded-wait self-test (include/rel_attn_profile.h)."""
-    if stream is None:
-        stream = torch.cuda.current_stream().cuda_stream
-    _check(lib.rel_attn_check_wait_timeout(int(timeout_ms), ctypes.c_void_p(stream)))
+    _check(lib.rel_attn_check_wait_timeout(int(timeout_ms), ctypes.c_void_p(_stream_handle(stream, None))))
