@@ -98,6 +98,11 @@ SMALL = [
          head_dim=128),
     dict(name="block32", seqlens_q=[2, 1], seqlens_k=[95, 200], num_heads=8, num_kv_heads=2, head_dim=128,
          block_size=32),
+    # each row sees only its own position (rows past a short cache see nothing)
+    dict(name="window_diagonal_only", seqlens_q=[3, 5], seqlens_k=[40, 3], num_heads=4, num_kv_heads=2,
+         head_dim=128, window=(0, 0)),
+    dict(name="window_left_noncausal", seqlens_q=[4], seqlens_k=[200], num_heads=8, num_kv_heads=2, head_dim=64,
+         causal=False, window=(20, -1)),
     dict(name="big_pool", seqlens_q=[1], seqlens_k=[1000], num_heads=8, num_kv_heads=8, head_dim=128,
          pool_blocks=400, extra_table_cols=5),
 ]

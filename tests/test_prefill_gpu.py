@@ -45,6 +45,11 @@ SMALL = [
     # four tokens per tile: one bias box holds all 32 heads of a 4-token sub-box
     dict(name="gqa32_four_tokens_per_tile", seqlens_q=[11, 6], seqlens_k=[400, 6], num_heads=64,
          num_kv_heads=2, head_dim=128, rel_extent=96),
+    # each row sees only its own position (rows past a short cache see nothing)
+    dict(name="window_diagonal_only", seqlens_q=[70, 40], seqlens_k=[70, 20], num_heads=4, num_kv_heads=2,
+         head_dim=128, window=(0, 0), rel_extent=8),
+    dict(name="window_left_noncausal", seqlens_q=[66], seqlens_k=[400], num_heads=4, num_kv_heads=2,
+         head_dim=64, causal=False, window=(100, -1), rel_extent=24),
     # one token per tile (every row of a tile is a head of the same token)
     dict(name="gqa128_one_token_per_tile", seqlens_q=[3, 2], seqlens_k=[260, 70], num_heads=128,
          num_kv_heads=1, head_dim=64, rel_extent=40),
