@@ -161,3 +161,22 @@ def test_prefill_compact_grid_with_inflated_max_seqlen_q():
     assert info["grid"][0] == 2 * ((T + 63) // 64 + 5)
     assert_close(got, ref.forward(c), what="inflated max_seqlen_q")
     assert_no_device_error()
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_prefill_strided_q_and_out_with_guard(splits):
+    """q as a view into a packed (T, H + 2 Hk, D) projection, out as a view of a
+    wider buffer: results match and nothing outside the out view is written."""
+    c = make_case(seed=61, seqlens_q=[70, 33], seqlens_k=[300, 120], num_heads=8, num_kv_heads=2, head_dim=128,
+                  rel_extent=24)
+    g = to_dev(c)
+    T, H, D = c.q.shape
+    qkv = torch.zeros(T, H + 4, D, dtype=torch.bfloat16, device="cuda")
+    qkv[:, :H] = g["q"]
+    g["q"] = qkv[:, :H]
+    big_o = torch.full((T, H, 2 * D), 7.0, dtype=torch.bfloat16, device="cuda")
+    out = big_o[:, :, D:]
+    run(c, g, out=out, num_splits=splits)
+    assert_close(out, ref.forward(c), what=f"strided prefill splits={splits}")
+    assert torch.all(big_o[:, :, :D] == 7.0)
+    assert_no_device_error()
