@@ -33,7 +33,8 @@ if ROOT not in sys.path:
 METRIC = "decode HBM TB/s & % roofline; prefill TFLOP/s & % bf16 peak (1×GB300)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DECODE = ("long_decode", "batched_decode", "tiny_mixed")
-KERNEL_SOURCES = {"decode": ["decode.cu", "common.cuh"], "prefill": ["prefill.cu", "common.cuh"]}
+KERNEL_SOURCES = {"decode": ["decode.cu", "common.cuh"], "prefill": ["prefill.cu", "common.cuh"],
+                  "append": ["append.cu", "common.cuh"]}
 
 
 def peaks():
@@ -396,7 +397,8 @@ def run_append(args, rank, world):
                    "num_kv_heads": d["Hk"], "head_dim": d["D"], "block_size": d["BS"],
                    "l2": "flushed (a 256 MB buffer read) before every launch", "algorithmic_bytes": nbytes},
         "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(ach / pk["hbm_gbs"], 4), "traffic": None,
+                     "frac": round(ach / pk["hbm_gbs"], 4),
+                     "traffic": recorded_traffic("append_chunked_prefill", "append"),
                      "peak_source": f"{pk_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"},
         "e2e": {"value": round(job_rate(world, nbytes, e2e_ms), 4), "unit": "TB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": rows, "d2h_bytes_per_step": 0,
