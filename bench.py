@@ -3,17 +3,26 @@
 One step = one rel_attn_paged_varlen call over the whole workload: the split
 heuristic, the main kernel and (when splits > 1) the LSE combine.  Inputs are
 seeded and synthetic (paged_attention_relative_gb300.workloads) and resident
-in HBM before timing; the KV cache (>= 512 MiB for the decode workloads) is
-larger than the 129 MB L2, so no flush is needed between steps.
+in HBM before timing; the attention inputs (KV cache >= 512 MiB for the
+decode workloads, 2.55 GB per chunked-prefill step) are larger than the
+129 MB L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
-`--workload append_chunked_prefill` times the paged KV-cache append instead
-(rel_attn_cache_append of the chunked-prefill workload's new tokens).
+The default run prints the long-decode headline (`value`) and, under
+"workloads", a complete record for each of the other measured workloads:
+batched decode, chunked prefill, mixed varlen with a window, and the paged
+KV-cache append of the chunked-prefill tokens.  Every record times its own
+steps after at least one second of back-to-back steps, with nvidia-smi
+sampling clocks over that whole busy period.  `--workload NAME` prints that
+workload's record alone.
 
 Prints one JSON line on rank 0.  Under torchrun every rank runs its own
 replica of the workload on its own GPU (the work shards by request and kv
-head with no exchange), so scaling is weak.
+head with no exchange), so scaling is weak.  The library is a one-GPU
+library and its prefill kernel loads K/V tiles with cluster multicast:
+multi-rank runs refuse the prefill workloads and leave them out of the
+default record.
 """
 from __future__ import annotations
 
@@ -32,7 +41,6 @@ if ROOT not in sys.path:
 
 METRIC = "decode HBM TB/s & % roofline; prefill TFLOP/s & % bf16 peak (1×GB300)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-DECODE = ("long_decode", "batched_decode", "tiny_mixed")
 KERNEL_SOURCES = {"decode": ["decode.cu", "common.cuh"], "prefill": ["prefill.cu", "common.cuh"],
                   "append": ["append.cu", "common.cuh"]}
 
@@ -155,19 +163,71 @@ def heuristic_splits(case, lib_splits):
                       d["Hk"], max(sk) if sk else 0)
 
 
-def run_ours(args, rank, world):
+PREFILL_MULTI_RANK = ("1-GPU library: the prefill kernel loads K/V tiles with cluster multicast, which runs on "
+                      "one GPU only; multi-rank runs time the decode workloads and the append")
+
+
+def uses_prefill(case) -> bool:
+    """The library picks the tcgen05 prefill kernel above 64 GQA-packed rows."""
+    d = case.dims
+    return case.max_seqlen_q * (d["H"] // d["Hk"]) > 64
+
+
+def soak_then_time(step, steps: int, soak_s: float, stream, dev, world):
+    """Run `step` back to back for about soak_s seconds (untimed), then time
+    exactly `steps` steps with CUDA events on `stream`, bracketed by a barrier
+    and a device synchronize; nvidia-smi samples clocks over the whole busy
+    period (so the samples see the GPU under load).  Returns (ms per step,
+    max over ranks; the clock summary; the soak's step count)."""
+    import torch
+    barrier = (lambda: torch.distributed.barrier()) if world > 1 else (lambda: None)
+    with ClockSampler(dev.index) as clocks:
+        t0 = time.perf_counter()
+        n_soak = 0
+        while True:
+            for _ in range(8):
+                step()
+            n_soak += 8
+            torch.cuda.synchronize()
+            if time.perf_counter() - t0 >= soak_s:
+                break
+        barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, world, dev)
+    summ = clocks.summary()
+    summ["window"] = f"{soak_s:g} s of back-to-back steps ({n_soak}) ending with the timed steps"
+    return ms, summ, n_soak
+
+
+def run_ours(args, rank, world, workload=None, steps=None, soak_s=1.0):
+    """One attention workload: device step time, the main kernel's time from
+    library-recorded events, end to end through the public API, roofline."""
+    import ctypes
+
     import torch
 
     import paged_attention_relative_gb300 as pa
     from paged_attention_relative_gb300 import _lib
     from paged_attention_relative_gb300.roofline import algorithmic_bytes, algorithmic_flops
 
+    workload = workload or args.workload
+    steps = steps or args.steps
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    case = make_workload(args.workload)
-    if args.splits is not None:
+    case = make_workload(workload)
+    if world > 1 and uses_prefill(case):
+        raise SystemExit(f"bench.py: {workload} refused with {world} ranks: {PREFILL_MULTI_RANK}")
+    if args.splits is not None and workload == args.workload:
         splits = args.splits
-    elif args.workload == "long_decode":
+    elif workload == "long_decode":
         splits = case.num_splits                  # the workload's own split count (16)
     else:
         splits = heuristic_splits(case, pa.rel_attn_num_splits)
@@ -181,7 +241,6 @@ def run_ours(args, rank, world):
                                        "cu_seqlens_q")]
     rel = _lib.describe(g["rel_logits"]) if case.rel_extent > 0 else None
     od = _lib.describe(out)
-    import ctypes
     refs = [ctypes.byref(d) for d in D]
     rref = ctypes.byref(rel) if rel is not None else None
     oref = ctypes.byref(od)
@@ -201,25 +260,11 @@ def run_ours(args, rank, world):
     info = pa.last_launch()
     kind = info["kernel"]
 
-    barrier = (lambda: torch.distributed.barrier()) if world > 1 else (lambda: None)
-
-    # Whole-step timing.
-    barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(dev.index) as clocks:
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-    barrier()
-    ms_total = max_over_ranks(e0.elapsed_time(e1), world, dev)
-    ms_step = ms_total / args.steps
+    # Whole-step timing after a soak of back-to-back steps.
+    ms_step, clocks, n_soak = soak_then_time(step, steps, soak_s, stream, dev, world)
 
     # Main-kernel timing with events recorded by the library around the launch.
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for b, e in evs:          # torch creates the CUDA event on first record
         b.record(stream)
         e.record(stream)
@@ -229,7 +274,7 @@ def run_ours(args, rank, world):
     pa.set_kernel_events(None, None)
     torch.cuda.synchronize()
     kern_ms = [b.elapsed_time(e) for b, e in evs]
-    kern_avg = sum(kern_ms) / len(kern_ms)
+    kern_avg = max_over_ranks(sum(kern_ms) / len(kern_ms), world, dev)
 
     # End to end through the public API: pinned host inputs -> device, call,
     # result -> pinned host, every step.  The paged KV cache stays resident.
@@ -267,15 +312,16 @@ def run_ours(args, rank, world):
     for _ in range(2):
         e2e_step()
     torch.cuda.synchronize()
-    barrier()
+    if world > 1:
+        torch.distributed.barrier()
     a0 = torch.cuda.Event(enable_timing=True)
     a1 = torch.cuda.Event(enable_timing=True)
     a0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         e2e_step()
     a1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(a0.elapsed_time(a1) / args.steps, world, dev)
+    e2e_ms = max_over_ranks(a0.elapsed_time(a1) / steps, world, dev)
 
     nbytes = algorithmic_bytes(case)
     flops = algorithmic_flops(case)
@@ -287,7 +333,7 @@ def run_ours(args, rank, world):
         e2e_value = job_rate(world, nbytes, e2e_ms)
         ach = nbytes / (kern_avg * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": round(ach / pk["hbm_gbs"], 4), "traffic": recorded_traffic(args.workload, kind),
+                "frac": round(ach / pk["hbm_gbs"], 4), "traffic": recorded_traffic(workload, kind),
                 "peak_source": f"{pk_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                 if pk_src == "measured" else "fallback 6.8 TB/s",
                 "nominal_frac_8tbs": round(ach / 8000.0, 4)}
@@ -297,18 +343,21 @@ def run_ours(args, rank, world):
         e2e_value = job_rate(world, flops, e2e_ms)
         ach = flops / (kern_avg * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(ach / pk["bf16_tflops"], 4), "traffic": recorded_traffic(args.workload, kind),
-                "peak_source": f"{pk_src} cuBLAS bf16 burst (MEASURED_PEAKS.json bf16_tflops)"}
+                "frac": round(ach / pk["bf16_tflops"], 4), "traffic": recorded_traffic(workload, kind),
+                "peak_source": f"{pk_src} cuBLAS bf16 burst (MEASURED_PEAKS.json bf16_tflops)",
+                "frac_of_sustained": round(ach / pk.get("bf16_tflops_sustained", pk["bf16_tflops"]), 4)}
     d = case.dims
     res = {
-        "metric": METRIC, "value": round(value, 4), "unit": unit, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": round(value, 4), "unit": unit, "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, shuffled page pool)",
-        "config": {"workload": args.workload, "batch": d["B"], "tokens": d["T"], "num_heads": d["H"],
+        "config": {"workload": workload, "batch": d["B"], "tokens": d["T"], "num_heads": d["H"],
                    "num_kv_heads": d["Hk"], "head_dim": d["D"], "block_size": d["BS"], "rel_extent": d["R"],
                    "max_kv_len": int(case.cache_seqlens.max()), "num_splits": splits,
                    "window": [case.window_left, case.window_right], "causal": case.causal,
-                   "parallelism": f"replicas{world}", "l2": "inputs larger than L2 (paged KV > 129 MB)",
+                   "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (paged KV > 129 MB)" if decode
+                   else "inputs larger than L2 (K/V, q and rel_logits > 129 MB)",
                    "algorithmic_bytes": nbytes, "algorithmic_flops": flops},
         "kernel": {"name": kind, "avg_ms": round(kern_avg, 5), "launches_per_step": info["launches"],
                    "grid": info["grid"], "block": info["block"], "smem_bytes": info["smem_bytes"]},
@@ -317,13 +366,15 @@ def run_ours(args, rank, world):
         "e2e": {"value": round(e2e_value, 4), "unit": unit, "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "pinned host q, rel_logits, block_table, cache_seqlens, cu_seqlens_q in (one packed copy); out back; paged KV resident"},
-        "gpu_launches": args.steps * info["launches"],
-        "clocks": clocks.summary(),
+        "gpu_launches": steps * info["launches"],
+        "clocks": clocks,
     }
+    del g, out, host_buf, dev_buf, host_out
+    torch.cuda.empty_cache()
     return res, case
 
 
-def run_append(args, rank, world):
+def run_append(args, rank, world, steps=None, soak_s=1.0):
     """The paged KV-cache append for the chunked-prefill workload's new tokens
     (4 x 4096 tokens, 8 kv heads, head_dim 128): HBM-bound, so `value` is
     algorithmic bytes (key and value rows read once and written once) per
@@ -333,6 +384,7 @@ def run_append(args, rank, world):
 
     import paged_attention_relative_gb300 as pa
 
+    steps = steps or args.steps
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     case = make_workload("chunked_prefill")
@@ -353,19 +405,28 @@ def run_append(args, rank, world):
     for _ in range(max(args.warmup, 3)):
         call(kd, vd)
     torch.cuda.synchronize()
-    # Events recorded by the library right around the launch (no host work inside).
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    # Events recorded by the library right around the launch (no host work
+    # inside), after a soak of flush + append steps under the clock sampler.
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for b, e in evs:          # torch creates the CUDA event on first record
         b.record(stream)
         e.record(stream)
     with ClockSampler(dev.index) as clocks:
+        t0 = time.perf_counter()
+        n_soak = 0
+        while time.perf_counter() - t0 < soak_s:
+            for _ in range(8):
+                flush.sum()
+                call(kd, vd)
+            n_soak += 8
+            torch.cuda.synchronize()
         for b, e in evs:
             flush.sum()
             pa.set_kernel_events(b, e)
             call(kd, vd)
         pa.set_kernel_events(None, None)
         torch.cuda.synchronize()
-    kern_ms = max_over_ranks(sum(b.elapsed_time(e) for b, e in evs) / args.steps, world, dev)
+    kern_ms = max_over_ranks(sum(b.elapsed_time(e) for b, e in evs) / steps, world, dev)
     rows = 2 * d["T"] * d["Hk"] * d["D"] * 2
     nbytes = 2 * rows + (d["B"] + 1) * 4 + d["B"] * 4 + d["T"] * 4  # rows in and out, lengths, a table entry per token
     pk, pk_src = peaks()
@@ -383,19 +444,22 @@ def run_append(args, rank, world):
     torch.cuda.synchronize()
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         e2e_step()
     a1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(a0.elapsed_time(a1) / args.steps, world, dev)
+    e2e_ms = max_over_ranks(a0.elapsed_time(a1) / steps, world, dev)
+    summ = clocks.summary()
+    summ["window"] = f"{soak_s:g} s of back-to-back flush + append steps ({n_soak}) ending with the timed launches"
     res = {
         "metric": "paged KV-cache append bandwidth", "value": round(job_rate(world, nbytes, kern_ms), 4),
-        "unit": "TB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "unit": "TB/s", "n_gpus": world, "steps": steps, "warmup": args.warmup,
         "ms_per_step": round(kern_ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 rows, shuffled page pool)",
         "config": {"workload": "append_chunked_prefill", "batch": d["B"], "tokens": d["T"],
                    "num_kv_heads": d["Hk"], "head_dim": d["D"], "block_size": d["BS"],
                    "l2": "flushed (a 256 MB buffer read) before every launch", "algorithmic_bytes": nbytes},
+        "kernel": {"name": "append", "avg_ms": round(kern_ms, 5), "launches_per_step": 1},
         "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": round(ach / pk["hbm_gbs"], 4),
                      "traffic": recorded_traffic("append_chunked_prefill", "append"),
@@ -403,8 +467,8 @@ def run_append(args, rank, world):
         "e2e": {"value": round(job_rate(world, nbytes, e2e_ms), 4), "unit": "TB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": rows, "d2h_bytes_per_step": 0,
                 "note": "pinned host key/value in, append; the product is the device cache (nothing read back)"},
-        "gpu_launches": args.steps,
-        "clocks": clocks.summary(),
+        "gpu_launches": steps,
+        "clocks": summ,
     }
     if rank == 0 and not args.no_cpu_baseline:
         from oracle import reference as ref
@@ -413,6 +477,8 @@ def run_append(args, rank, world):
         s = time.perf_counter() - t0
         res["cpu_baseline"] = {"value": round(nbytes / s / 1e12, 6), "unit": "TB/s", "cores": 1, "kind": "oracle",
                                "sample": "the whole write (every token), once", "seconds_per_step": round(s, 3)}
+    del g, kd, vd, flush
+    torch.cuda.empty_cache()
     return res
 
 
@@ -444,6 +510,20 @@ def time_oracle(case, budget_s: float, cores: int | None = None):
     return full, f"{done} of {n_rows} (token, head) output rows in a random order (seed 0), scaled to the whole workload", cores
 
 
+def add_cpu_baseline(res, case, budget_s: float, single_core_s: float = 0.0):
+    full_s, sample, cores = time_oracle(case, budget_s)
+    unit_work = res["config"]["algorithmic_bytes"] if res["unit"] == "TB/s" else res["config"]["algorithmic_flops"]
+    res["cpu_baseline"] = {"value": round(unit_work / full_s / 1e12, 6), "unit": res["unit"], "cores": cores,
+                           "kind": "oracle", "sample": sample, "seconds_per_step": round(full_s, 3)}
+    if single_core_s > 0:
+        one_s, one_sample, _ = time_oracle(case, single_core_s, cores=1)
+        res["cpu_baseline"]["single_core"] = {"value": round(unit_work / one_s / 1e12, 6), "cores": 1,
+                                              "sample": one_sample, "seconds_per_step": round(one_s, 3)}
+
+
+SUB_WORKLOADS = ("batched_decode", "chunked_prefill", "mixed_window", "append_chunked_prefill")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -453,7 +533,13 @@ def main():
     ap.add_argument("--splits", type=int, default=None)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--sub-cpu-budget", type=float, default=4.0,
+                    help="seconds of oracle work for each sub-record's cpu_baseline")
+    ap.add_argument("--soak-s", type=float, default=1.0,
+                    help="seconds of back-to-back steps (clock-sampled) before each timed region")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub-workloads", action="store_true",
+                    help="print the headline workload's record only")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -464,27 +550,40 @@ def main():
         run_reference(args, rank, world)
         return
 
+    if world > 1 and args.workload in ("chunked_prefill", "mixed_window"):
+        if rank == 0:
+            print(f"bench.py: --workload {args.workload} refused with {world} ranks: {PREFILL_MULTI_RANK}",
+                  file=sys.stderr, flush=True)
+        sys.exit(2)
+
     if world > 1:
         import torch
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         torch.distributed.init_process_group("nccl")
     if args.workload == "append_chunked_prefill":
-        res = run_append(args, rank, world)
-        if rank == 0:
-            print(json.dumps(res), flush=True)
-        if world > 1:
-            import torch
-            torch.distributed.destroy_process_group()
-        return
-    res, case = run_ours(args, rank, world)
-    if rank == 0 and not args.no_cpu_baseline:
-        full_s, sample, cores = time_oracle(case, args.cpu_budget)
-        unit_work = res["config"]["algorithmic_bytes"] if res["unit"] == "TB/s" else res["config"]["algorithmic_flops"]
-        res["cpu_baseline"] = {"value": round(unit_work / full_s / 1e12, 6), "unit": res["unit"], "cores": cores,
-                               "kind": "oracle", "sample": sample, "seconds_per_step": round(full_s, 3)}
-        one_s, one_sample, _ = time_oracle(case, min(4.0, args.cpu_budget), cores=1)
-        res["cpu_baseline"]["single_core"] = {"value": round(unit_work / one_s / 1e12, 6), "cores": 1,
-                                              "sample": one_sample, "seconds_per_step": round(one_s, 3)}
+        res = run_append(args, rank, world, soak_s=args.soak_s)
+    else:
+        res, case = run_ours(args, rank, world, soak_s=args.soak_s)
+        if rank == 0 and not args.no_cpu_baseline:
+            add_cpu_baseline(res, case, args.cpu_budget, min(4.0, args.cpu_budget))
+    default_run = args.workload == "long_decode" and not args.no_sub_workloads and args.splits is None
+    if default_run:
+        subs, skipped = {}, {}
+        for name in SUB_WORKLOADS:
+            if name == "append_chunked_prefill":
+                subs[name] = run_append(args, rank, world, soak_s=args.soak_s)
+                continue
+            if world > 1 and name in ("chunked_prefill", "mixed_window"):
+                skipped[name] = PREFILL_MULTI_RANK
+                continue
+            sub, sub_case = run_ours(args, rank, world, workload=name, soak_s=args.soak_s)
+            if rank == 0 and not args.no_cpu_baseline:
+                add_cpu_baseline(sub, sub_case, args.sub_cpu_budget)
+            subs[name] = sub
+        res["workloads"] = subs
+        if skipped:
+            res["workloads_skipped"] = skipped
+        res["gpu_launches_all_records"] = res["gpu_launches"] + sum(r["gpu_launches"] for r in subs.values())
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

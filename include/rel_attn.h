@@ -109,7 +109,12 @@ typedef enum {
  * Errors: REL_ATTN_ERR_INVALID_ARGUMENT for a NULL pointer with a nonzero
  * size, a dtype/rank/shape/stride mismatch, H % Hk != 0, num_splits < 1 or
  * rel_extent < 0; REL_ATTN_ERR_UNSUPPORTED for another D or BS, a device that
- * is not sm_103, or a layout TMA cannot address; REL_ATTN_ERR_OUT_OF_MEMORY
+ * is not sm_103, a layout TMA cannot address, or a tensor that is not device
+ * memory of the current device (host memory, another GPU's memory; checked
+ * with cudaPointerGetAttributes before any tensor map is encoded; q, out,
+ * block_table, cache_seqlens, cu_seqlens_q and softmax_lse may also be
+ * managed memory, the caches and rel_logits, read by TMA, may not);
+ * REL_ATTN_ERR_OUT_OF_MEMORY
  * when the workspace cannot be allocated; REL_ATTN_ERR_CUDA for a launch
  * error.  rel_attn_last_error() then describes it.  T == 0 returns OK and
  * launches nothing.  Device-side preconditions (monotone cu_seqlens_q,
@@ -117,6 +122,9 @@ typedef enum {
  * checked, unless the environment variable REL_ATTN_CHECK=1 is set, in which
  * case a check kernel runs first, the call synchronises `stream`, and a
  * violation returns REL_ATTN_ERR_DEVICE_CHECK without running the forward.
+ * Without the check, a block id outside [0, NB) is clamped into the cache and
+ * a key past the table's width reads no table entry, so a broken table gives
+ * wrong values, never a read outside the caches.
  */
 rel_attn_status rel_attn_paged_varlen(
     const rel_attn_tensor* q,
@@ -178,33 +186,35 @@ rel_attn_status rel_attn_paged_varlen_lse(
     rel_attn_stream stream);
 
 /*
- * rel_attn_paged_varlen_noalloc - the same forward for the decode path
- * (max_seqlen_q * num_heads / num_kv_heads <= 64) that allocates no device
- * memory.  It has no counterpart on the pages that define the attention; it
- * exists for callers that cannot allocate: a framework that owns the device
- * through its own memory pool (a second allocator working behind its back can
- * run out of memory while the pool holds nearly all of the device, or
- * fragment it), or a program that allocates everything at start-up and
- * forbids allocation afterwards.
+ * rel_attn_paged_varlen_noalloc - rel_attn_paged_varlen that allocates no
+ * device memory.  It has no counterpart on the pages that define the
+ * attention; it exists for callers that cannot allocate: a framework that owns
+ * the device through its own memory pool (a second allocator working behind
+ * its back can run out of memory while the pool holds nearly all of the
+ * device, or fragment it), or a program that allocates everything at start-up
+ * and forbids allocation afterwards.
  *
- * Arguments, results and errors are those of rel_attn_paged_varlen.  The
- * caller still provides every input and the output.  The split-KV workspace
- * (num_splits * T * H * (D + 1) * 4 bytes, after num_splits is clamped) comes
- * from a fixed array of REL_ATTN_NOALLOC_SCRATCH_BYTES bytes inside the
- * library; every GPU that loads the library holds one such array until the
- * process exits.  A call whose workspace would not fit returns
+ * Arguments, validation, status codes, kernels, the REL_ATTN_CHECK device
+ * check, the wait timeout and the launch record are those of
+ * rel_attn_paged_varlen (one shared implementation, decode and prefill path
+ * alike).  The caller still provides every input and the output.  The only
+ * difference is the split-KV workspace (num_splits * T * H * (D + 1) * 4
+ * bytes, after num_splits is clamped; none with one split): it comes from a
+ * fixed array of REL_ATTN_NOALLOC_SCRATCH_BYTES bytes inside the library, and
+ * every GPU that loads the library holds one such array until the process
+ * exits.  A call whose workspace would not fit returns
  * REL_ATTN_ERR_INVALID_ARGUMENT with a message naming both sizes, before any
- * device work; so does a call on the prefill path
- * (REL_ATTN_ERR_UNSUPPORTED).  It calls no cudaMalloc, cudaMallocAsync,
- * cudaFree or other allocating routine.
+ * device work.  It calls no cudaMalloc, cudaMallocAsync, cudaFree or other
+ * allocating routine.
  *
- * The first call on each device looks up the device address of the array
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  All calls share the one array and it keeps the
- * last call's contents; nothing in it needs to start at zero, since every
- * value the combine step reads is written earlier in the same call.  Calls
- * that use more than one split and overlap on the GPU (other streams, other
- * host threads) race on the array: order them on one stream.
+ * The first call on each device that passes host validation looks up the
+ * device address of the array (cudaGetSymbolAddress, with that device
+ * current); make that first call before any stream capture.  All calls share
+ * the one array and it keeps the last call's contents; nothing in it needs to
+ * start at zero, since every value the combine step reads is written earlier
+ * in the same call.  Calls that use more than one split and overlap on the
+ * GPU (other streams, other host threads) race on the array: order them on
+ * one stream.
  */
 #define REL_ATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
 
@@ -261,10 +271,15 @@ rel_attn_status rel_attn_paged_varlen_noalloc(
  * otherwise which write lands is unspecified.
  * Errors: REL_ATTN_ERR_INVALID_ARGUMENT for a NULL pointer with a nonzero size,
  * a dtype/rank/shape/stride mismatch, or key/value overlapping a cache;
- * REL_ATTN_ERR_UNSUPPORTED for a D it cannot copy, misaligned data or a device
- * that is not sm_103; REL_ATTN_ERR_CUDA for a launch error.  T == 0 is a
- * no-op.  Device-side preconditions as for rel_attn_paged_varlen (checked when
- * REL_ATTN_CHECK=1).
+ * REL_ATTN_ERR_UNSUPPORTED for a D it cannot copy, misaligned data, a tensor
+ * that is not device memory of the current device, or a device that is not
+ * sm_103; REL_ATTN_ERR_CUDA for a launch error.  T == 0 is a no-op.
+ * Device-side preconditions as for rel_attn_paged_varlen (checked when
+ * REL_ATTN_CHECK=1).  Without the check, a token whose slot lies past the
+ * table's width (pos / BS >= MB) or in a block id outside [0, NB) is not
+ * written (a write is never clamped into another slot) and the device error
+ * word (rel_attn_device_error, rel_attn_profile.h) records
+ * REL_ATTN_CODE_APPEND_SLOT.
  */
 rel_attn_status rel_attn_cache_append(
     const rel_attn_tensor* key,

@@ -47,13 +47,17 @@ rel_attn_status rel_attn_set_kernel_events(void* begin, void* end);
 /*
  * Synchronise the current device, then read and clear the device error word
  * that the kernels set when a bounded wait on an mbarrier runs out (0 = none;
- * otherwise a code naming the wait site).  Kernels that time out return early
+ * otherwise a code naming the wait site) or when the cache append skips a
+ * token without a valid slot (REL_ATTN_CODE_APPEND_SLOT).  Kernels that time out return early
  * instead of hanging; their outputs are then undefined.
  */
 rel_attn_status rel_attn_device_error(int32_t* code);
 
 /* Wait-site code that rel_attn_check_wait_timeout records. */
 #define REL_ATTN_SITE_SELF_TEST 99
+/* Code the cache append records when it skips a token whose slot lies
+ * outside the block table or the cache. */
+#define REL_ATTN_CODE_APPEND_SLOT 31
 
 /*
  * Self-test of the bounded-wait path: launch on `stream` a one-thread kernel

@@ -44,6 +44,7 @@ rel_attn_status fail(rel_attn_status st, const char* fmt, ...) {
 
 struct DeviceInfo {
     bool ready = false;
+    int ordinal = 0;
     int major = 0, minor = 0, sms = 0;
     int* err = nullptr;
     int* check_err = nullptr;
@@ -64,6 +65,7 @@ rel_attn_status device_info(DeviceInfo** out) {
         cudaDeviceProp prop;
         e = cudaGetDeviceProperties(&prop, dev);
         if (e != cudaSuccess) return fail(REL_ATTN_ERR_CUDA, "cudaGetDeviceProperties: %s", cudaGetErrorString(e));
+        d.ordinal = dev;
         d.major = prop.major;
         d.minor = prop.minor;
         d.sms = prop.multiProcessorCount;
@@ -159,6 +161,26 @@ bool overlaps(const rel_attn_tensor* a, int ea, const rel_attn_tensor* b, int eb
     if (na == 0 || nb == 0) return false;
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(a->data), b0 = reinterpret_cast<uintptr_t>(b->data);
     return a0 < b0 + (uintptr_t)nb && b0 < a0 + (uintptr_t)na;
+}
+
+// Every tensor the kernels touch must be device memory of the current device:
+// the tensor maps and the kernels' loads address it directly, so memory of
+// another GPU or of the host is rejected before anything is encoded or
+// launched.  `tma` tensors (read through tensor maps) must be plain device
+// allocations; the others may also be managed memory.
+rel_attn_status check_resident(const rel_attn_tensor* t, const char* name, int dev, bool tma) {
+    if (!t || !t->data) return REL_ATTN_OK;
+    cudaPointerAttributes a{};
+    const cudaError_t e = cudaPointerGetAttributes(&a, t->data);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(REL_ATTN_ERR_UNSUPPORTED, "%s: not a CUDA allocation (%s)", name, cudaGetErrorString(e));
+    }
+    const bool on_dev = a.type == cudaMemoryTypeDevice && a.device == dev;
+    if (!(on_dev || (!tma && a.type == cudaMemoryTypeManaged)))
+        return fail(REL_ATTN_ERR_UNSUPPORTED, "%s is not device memory of the current device %d (memory type %d, device %d)",
+                    name, dev, (int)a.type, a.device);
+    return REL_ATTN_OK;
 }
 
 uint64_t wait_timeout_ns() {
@@ -305,15 +327,17 @@ extern "C" rel_attn_status rel_attn_device_error(int32_t* code) {
     return REL_ATTN_OK;
 }
 
-namespace {
+namespace relattn {
 
-// Body of rel_attn_paged_varlen and rel_attn_paged_varlen_lse (lse may be NULL).
+// Body of rel_attn_paged_varlen, rel_attn_paged_varlen_lse (lse may be NULL)
+// and rel_attn_paged_varlen_noalloc (fixed_ws non-NULL: the split workspace
+// is that buffer, and a call needing more is rejected before any device work).
 rel_attn_status paged_varlen(
     const rel_attn_tensor* q, const rel_attn_tensor* key_cache, const rel_attn_tensor* value_cache,
     const rel_attn_tensor* block_table, const rel_attn_tensor* cache_seqlens, const rel_attn_tensor* cu_seqlens_q,
     int32_t max_seqlen_q, float softmax_scale, int32_t causal, int32_t window_left, int32_t window_right,
     int32_t rel_extent, const rel_attn_tensor* rel_logits, int32_t num_splits, rel_attn_tensor* out,
-    rel_attn_tensor* lse, rel_attn_stream stream_) {
+    rel_attn_tensor* lse, rel_attn_stream stream_, const FixedWorkspace* fixed_ws) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     t_launch = rel_attn_launch_info{};
     rel_attn_status st;
@@ -406,10 +430,36 @@ rel_attn_status paged_varlen(
     if ((st = device_info(&dev))) return st;
     if (dev->major != 10 || dev->minor != 3)
         return fail(REL_ATTN_ERR_UNSUPPORTED, "built for sm_103a; device is sm_%d%d", dev->major, dev->minor);
+    if ((st = check_resident(q, "q", dev->ordinal, false)) ||
+        (st = check_resident(key_cache, "key_cache", dev->ordinal, true)) ||
+        (st = check_resident(value_cache, "value_cache", dev->ordinal, true)) ||
+        (st = check_resident(block_table, "block_table", dev->ordinal, false)) ||
+        (st = check_resident(cache_seqlens, "cache_seqlens", dev->ordinal, false)) ||
+        (st = check_resident(cu_seqlens_q, "cu_seqlens_q", dev->ordinal, false)) ||
+        (rel_extent > 0 && (st = check_resident(rel_logits, "rel_logits", dev->ordinal, true))) ||
+        (st = check_resident(out, "out", dev->ordinal, false)) ||
+        (lse && (st = check_resident(lse, "softmax_lse", dev->ordinal, false))))
+        return st;
 
     const int64_t G = H / Hk;
     const int64_t rows = (int64_t)max_seqlen_q * G;
     const bool prefill = rows > 64;  // decode kernel up to 64 packed rows, tcgen05 tiles above
+
+    // Splits: a cap, clamped to the 16-key slices a request can have.
+    int64_t splits = num_splits;
+    const int64_t slice_cap = (MB * BS + 15) / 16;
+    if (splits > slice_cap) splits = slice_cap < 1 ? 1 : slice_cap;
+    if (splits > 1024) splits = 1024;
+    const size_t ws_bytes = splits > 1 ? (size_t)splits * T * H * (D + 1) * sizeof(float) : 0;
+    if (fixed_ws && ws_bytes > fixed_ws->bytes)
+        return fail(REL_ATTN_ERR_INVALID_ARGUMENT,
+                    "the split workspace needs %zu bytes, more than the %zu-byte static scratch; lower num_splits "
+                    "or call rel_attn_paged_varlen",
+                    ws_bytes, fixed_ws->bytes);
+    // The fixed workspace's device address on this device (looked up once
+    // per device, on the first call that gets this far).
+    void* fixed_base = nullptr;
+    if (fixed_ws && (st = fixed_ws->address(&fixed_base))) return st;
 
     if (check_enabled() && (st = run_device_check(dev, stream, cu_seqlens_q, cache_seqlens, block_table, B, T, MB,
                                                    BS, NB, max_seqlen_q)))
@@ -476,25 +526,25 @@ rel_attn_status paged_varlen(
         if (p.vec_bias && (st = make_rel_map(rel_logits, (int)G, ts, &maps[2]))) return st;
     }
 
-    // Splits: a cap, clamped to the 16-key slices a request can have.
-    int64_t max_keys = MB * BS;
-    int64_t splits = num_splits;
-    const int64_t slice_cap = (max_keys + 15) / 16;
-    if (splits > slice_cap) splits = slice_cap < 1 ? 1 : slice_cap;
-    if (splits > 1024) splits = 1024;
     p.num_splits = (int32_t)splits;
 
+    // The split workspace: the caller's fixed buffer, else a stream-ordered
+    // allocation freed after the combine.
     void* ws = nullptr;
-    size_t ws_bytes = 0;
     if (splits > 1) {
-        ws_bytes = (size_t)splits * T * H * (D + 1) * sizeof(float);
-        cudaError_t e = cudaMallocAsync(&ws, ws_bytes, stream);
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            return fail(e == cudaErrorMemoryAllocation ? REL_ATTN_ERR_OUT_OF_MEMORY : REL_ATTN_ERR_CUDA,
-                        "split workspace of %zu bytes: %s", ws_bytes, cudaGetErrorString(e));
+        void* base = nullptr;
+        if (fixed_ws) {
+            base = fixed_base;
+        } else {
+            cudaError_t e = cudaMallocAsync(&ws, ws_bytes, stream);
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                return fail(e == cudaErrorMemoryAllocation ? REL_ATTN_ERR_OUT_OF_MEMORY : REL_ATTN_ERR_CUDA,
+                            "split workspace of %zu bytes: %s", ws_bytes, cudaGetErrorString(e));
+            }
+            base = ws;
         }
-        p.ws_o = static_cast<float*>(ws);
+        p.ws_o = static_cast<float*>(base);
         p.ws_lse = p.ws_o + (size_t)splits * T * H * D;
     }
 
@@ -526,7 +576,7 @@ rel_attn_status paged_varlen(
     return REL_ATTN_OK;
 }
 
-}  // namespace
+}  // namespace relattn
 
 extern "C" rel_attn_status rel_attn_paged_varlen(
     const rel_attn_tensor* q, const rel_attn_tensor* key_cache, const rel_attn_tensor* value_cache,
@@ -536,7 +586,7 @@ extern "C" rel_attn_status rel_attn_paged_varlen(
     rel_attn_stream stream) {
     return paged_varlen(q, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_q, max_seqlen_q,
                         softmax_scale, causal, window_left, window_right, rel_extent, rel_logits, num_splits, out,
-                        nullptr, stream);
+                        nullptr, stream, nullptr);
 }
 
 extern "C" rel_attn_status rel_attn_paged_varlen_lse(
@@ -547,7 +597,7 @@ extern "C" rel_attn_status rel_attn_paged_varlen_lse(
     rel_attn_tensor* softmax_lse, rel_attn_stream stream) {
     return paged_varlen(q, key_cache, value_cache, block_table, cache_seqlens, cu_seqlens_q, max_seqlen_q,
                         softmax_scale, causal, window_left, window_right, rel_extent, rel_logits, num_splits, out,
-                        softmax_lse, stream);
+                        softmax_lse, stream, nullptr);
 }
 
 namespace relattn {
@@ -622,6 +672,14 @@ extern "C" rel_attn_status rel_attn_cache_append(
     if ((st = device_info(&dev))) return st;
     if (dev->major != 10 || dev->minor != 3)
         return fail(REL_ATTN_ERR_UNSUPPORTED, "built for sm_103a; device is sm_%d%d", dev->major, dev->minor);
+    if ((st = check_resident(key, "key", dev->ordinal, false)) ||
+        (st = check_resident(value, "value", dev->ordinal, false)) ||
+        (st = check_resident(key_cache, "key_cache", dev->ordinal, false)) ||
+        (st = check_resident(value_cache, "value_cache", dev->ordinal, false)) ||
+        (st = check_resident(block_table, "block_table", dev->ordinal, false)) ||
+        (st = check_resident(cache_seqlens, "cache_seqlens", dev->ordinal, false)) ||
+        (st = check_resident(cu_seqlens_q, "cu_seqlens_q", dev->ordinal, false)))
+        return st;
     if (check_enabled() && (st = run_device_check(dev, stream, cu_seqlens_q, cache_seqlens, block_table, B, T, MB,
                                                    BS, NB, (int)T)))
         return st;
@@ -646,6 +704,9 @@ extern "C" rel_attn_status rel_attn_cache_append(
     p.Hk = (int32_t)Hk;
     p.BS = (int32_t)BS;
     p.D = (int32_t)D;
+    p.MB = (int32_t)MB;
+    p.NB = (int32_t)NB;
+    p.err = dev->err;
     if (t_ev_begin) cudaEventRecord(t_ev_begin, stream);
     cudaError_t e = launch_append(p, stream);
     if (t_ev_end) cudaEventRecord(t_ev_end, stream);

@@ -9,7 +9,8 @@
 //   (value likewise),  pos = cache_seqlens[b] - sq_b + i,
 //
 // and a token with pos < 0 (cache_seqlens[b] < sq_b) has no slot and is
-// skipped.  One warp per token: it finds the token's request with one
+// skipped; so is a token whose slot lies past the table's width or in a
+// block outside the cache (recorded in the device error word).  One warp per token: it finds the token's request with one
 // parallel read of cu_seqlens_q and cache_seqlens (32 requests per read) and
 // a ballot, reads the block id, then moves all kv heads of K and V in
 // 16-byte pieces.
@@ -50,7 +51,19 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
     const int sq = q1 - q0;
     const int pos = skb - sq + (int)(t - q0);
     if (pos < 0) return;
-    const int blk = __ldg(p.block_table + (size_t)b * p.bt_stride + pos / p.BS);
+    // A slot past the block table's width or a block id outside the cache
+    // breaks the caller's contract: the token is not written (a write is
+    // never clamped into another slot) and the device error word says so.
+    const int n = pos / p.BS;
+    if (n >= p.MB) {
+        if (lane == 0) atomicCAS(p.err, 0, kCodeAppendSlot);
+        return;
+    }
+    const int blk = __ldg(p.block_table + (size_t)b * p.bt_stride + n);
+    if (blk < 0 || blk >= p.NB) {
+        if (lane == 0) atomicCAS(p.err, 0, kCodeAppendSlot);
+        return;
+    }
     const long long dst_row = (long long)blk * p.c_s0 + (long long)(pos % p.BS) * p.c_s1;
     const int chunks = p.D / 8;  // 16-byte pieces per (token, head) row
     const int per_tensor = p.Hk * chunks;

@@ -25,6 +25,7 @@ enum WaitSite : int {
     kSitePrefillRelEmpty = 19,
     kSitePrefillSEmpty = 20,
     kSitePrefillXchg = 21,
+    kCodeAppendSlot = 31,  // cache append: a token's slot lies outside the block table or the cache (skipped)
     kSiteSelfTest = 99,  // rel_attn_check_wait_timeout
 };
 
@@ -42,6 +43,26 @@ __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Softmax weights independent of the split partition.  Both attention
+// kernels keep every row's reference maximum m at an integer in log2 units
+// and quantise each score y (log2 units) to a fixed absolute grid before
+// subtracting it: adding kQuantC rounds y to a multiple of 2^-16 for
+// |y| < 64 (of a coarser power of two beyond), subtracting kQuantC + m is
+// then exact.  A weight 2^(y_q - m) therefore depends on the reference only
+// through an exact power of two, its bf16 rounding is the same for every
+// reference, and a split-KV result differs from the one-split result only by
+// fp32 summation order, not by how P was rounded.  The quantisation moves a
+// weight by at most a relative 2^-17 * ln 2.
+constexpr float kQuantC = 192.0f;  // 1.5 * 2^7: y + kQuantC lies in [128, 256) for |y| < 64
+
+// The integer reference for a row maximum mx (log2 units): ceil(mx), or -inf.
+__device__ __forceinline__ float ref_max(float mx) { return ceilf(mx); }
+
+// 2^n, exact, for an integer-valued n <= 127; 0 below 2^-126 (and for -inf).
+__device__ __forceinline__ float exp2_int(float n) {
+    return n < -126.f ? 0.f : __int_as_float(((int)n + 127) << 23);
 }
 
 // ---------------------------------------------------------------- mbarrier

@@ -222,9 +222,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, KSL>::kMaxThreads) decode_ker
     float o[D / 8][4];
 #pragma unroll
     for (int a = 0; a < D / 8; ++a) o[a][0] = o[a][1] = o[a][2] = o[a][3] = 0.f;
-    // m_run: running maximum of each row (log2 domain).  O and l are rescaled
-    // only in slices where some row of the warp raised its maximum; the row's
-    // largest p is then exactly 1, so its bf16 rounding is exact.
+    // m_run: reference maximum of each row, an integer in log2 units (the
+    // ceiling of the running maximum; see kQuantC: weights then do not
+    // depend on the split partition).  O and l are rescaled, by an exact
+    // power of two, only in slices where some row of the warp exceeded it.
     float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};
     float l_run[2] = {0.f, 0.f};
     const float sl2 = p.scale_log2;
@@ -315,8 +316,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, KSL>::kMaxThreads) decode_ker
             float alpha[2];
 #pragma unroll
             for (int rsel = 0; rsel < 2; ++rsel) {
-                const float m_new = fmaxf(m_run[rsel], mx[rsel]);
-                alpha[rsel] = m_new == -CUDART_INF_F ? 1.f : ex2(m_run[rsel] - m_new);
+                const float m_new = fmaxf(m_run[rsel], ref_max(mx[rsel]));
+                alpha[rsel] = m_new == -CUDART_INF_F ? 1.f : exp2_int(m_run[rsel] - m_new);
                 l_run[rsel] *= alpha[rsel];
                 m_run[rsel] = m_new;
             }
@@ -330,12 +331,13 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, KSL>::kMaxThreads) decode_ker
         }
 #pragma unroll
         for (int rsel = 0; rsel < 2; ++rsel) {
-            const float mu = m_run[rsel] == -CUDART_INF_F ? 0.f : m_run[rsel];
+            // 2^(q(s) - m): s quantised on the fixed grid, the subtraction exact.
+            const float off = kQuantC + (m_run[rsel] == -CUDART_INF_F ? 0.f : m_run[rsel]);
             float rs = 0.f;
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
-                s[nt][2 * rsel] = ex2(s[nt][2 * rsel] - mu);
-                s[nt][2 * rsel + 1] = ex2(s[nt][2 * rsel + 1] - mu);
+                s[nt][2 * rsel] = ex2((s[nt][2 * rsel] + kQuantC) - off);
+                s[nt][2 * rsel + 1] = ex2((s[nt][2 * rsel + 1] + kQuantC) - off);
                 rs += s[nt][2 * rsel] + s[nt][2 * rsel + 1];
             }
             l_run[rsel] += rs;
@@ -406,7 +408,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, KSL>::kMaxThreads) decode_ker
         if (M != -CUDART_INF_F) {
 #pragma unroll
             for (int k = 0; k < KSL; ++k) {
-                const float w = ex2(red_m[k * rows_cta + r] - M);
+                const float w = exp2_int(red_m[k * rows_cta + r] - M);  // integers: an exact power of two
                 L += w * red_l[k * rows_cta + r];
                 const float4 v =
                     *reinterpret_cast<const float4*>(red_o + ((size_t)k * rows_cta + r) * C::kRedStride + c4 * 4);

@@ -3,7 +3,10 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
+
+#include "rel_attn.h"
 
 namespace relattn {
 
@@ -82,10 +85,36 @@ struct AppendParams {
     const int32_t* cache_seqlens;
     const int32_t* cu_seqlens_q;
     int32_t B, T, Hk, BS, D;
+    int32_t MB;                // block_table width
+    int32_t NB;                // blocks in each cache
+    int* err;                  // device error word: a token whose slot is outside the table or cache
 };
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
 
 // LSE-weighted merge of split partials into out (and lse when requested).
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t stream);
+
+// A fixed device buffer of `bytes` bytes that serves as the split workspace
+// instead of a stream-ordered allocation (the allocation-free entry point).
+// `address` returns its device address on the current device; the body calls
+// it once host validation has passed, with the call's device current.
+struct FixedWorkspace {
+    rel_attn_status (*address)(void** ptr);
+    size_t bytes;
+};
+
+// The attention entry points' common body (api.cu): validation, kernel
+// choice, workspace, launches.  lse may be NULL; fixed_ws NULL allocates the
+// split workspace on `stream`.
+rel_attn_status paged_varlen(const rel_attn_tensor* q, const rel_attn_tensor* key_cache,
+                             const rel_attn_tensor* value_cache, const rel_attn_tensor* block_table,
+                             const rel_attn_tensor* cache_seqlens, const rel_attn_tensor* cu_seqlens_q,
+                             int32_t max_seqlen_q, float softmax_scale, int32_t causal, int32_t window_left,
+                             int32_t window_right, int32_t rel_extent, const rel_attn_tensor* rel_logits,
+                             int32_t num_splits, rel_attn_tensor* out, rel_attn_tensor* lse, rel_attn_stream stream,
+                             const FixedWorkspace* fixed_ws);
+
+// Set the thread-local message rel_attn_last_error() returns.
+void set_last_error_message(const char* msg);
 
 }  // namespace relattn

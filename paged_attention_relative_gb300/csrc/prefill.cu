@@ -46,8 +46,10 @@
 //              reference maximum while the partner's arrives, writes it into
 //              TMEM as bf16 pairs, rescales its half of the O row when the
 //              reference moved, and writes its half of the output.  The
-//              reference maximum moves lazily (only when the row maximum
-//              exceeds it by more than 2^8), so O is rarely rescaled.  The
+//              reference maximum is an integer in log2 units (so weights do
+//              not depend on the split partition, see kQuantC) and moves
+//              lazily (only when the row maximum exceeds it by more than
+//              2^8), so O is rarely rescaled.  The
 //              bias of a band tile is staged by warp 1: one 152-value window
 //              per (token, head) row, starting at the 16-byte aligned
 //              distance below the row's token sub-box, zero outside [0, R),
@@ -76,8 +78,8 @@ namespace relattn {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-// Lazy rescaling threshold: 8 in log2 units, in natural units.
-constexpr float kLazyRescale = 8.0f * 0.6931471805599453f;
+// Lazy rescaling threshold in log2 units.
+constexpr float kLazyRescale = 8.0f;
 // CTAs per cluster: adjacent query tiles that share (multicast) every K/V tile.
 constexpr int kCluster = 2;
 
@@ -339,7 +341,9 @@ __global__ void __launch_bounds__(384, 1)
             const int jw = w0 + (lane >> 3);
             if (jw < n_it) {
                 const int jg = key_block(jw) * C::BN + 16 * (lane & 7);
-                if (jg + 15 >= lo && jg < hi) v = __ldg(bt + jg / p.BS);
+                // (a key past the table's width, i.e. cache_seqlens > MB * BS,
+                // reads no entry: the clamp below then keeps block 0)
+                if (jg + 15 >= lo && jg < hi && jg / p.BS < p.max_blocks) v = __ldg(bt + jg / p.BS);
             }
             return v;
         };
@@ -569,7 +573,7 @@ __global__ void __launch_bounds__(384, 1)
         const float sl2 = p.scale_log2;    // sc * log2(e)
         const bool pos_scale = sc > 0.f;
         const int kh = 64 * half;  // first key of this half within a tile
-        float m_run = -CUDART_INF_F, l_half = 0.f;
+        float m_run = -CUDART_INF_F, l_half = 0.f;  // reference maximum (an integer in log2 units), half-row sum
         bool any_abort = false;
 
         // Warps 4-7 copy the Q tile into TMEM: row r to lane r, bf16 pairs per
@@ -719,16 +723,19 @@ __global__ void __launch_bounds__(384, 1)
             const float c1 = raw ? sl2 : kLog2e;
             uint32_t w[32];
             float rsum = 0.f;
-            // This half of P_j (bf16 pairs) and its row sum against reference m.
+            // This half of P_j (bf16 pairs) and its row sum against the
+            // integer reference m (log2 units): 2^(q(s * c1) - m), with the
+            // score quantised on a fixed grid so that the subtraction is exact.
             auto exp_pass = [&](float m) {
-                const float ml = m == -CUDART_INF_F ? 0.f : m * kLog2e;
-                const float2 c12 = make_float2(c1, c1), nml = make_float2(-ml, -ml);
+                const float off = kQuantC + (m == -CUDART_INF_F ? 0.f : m);
+                const float2 c12 = make_float2(c1, c1), qc = make_float2(kQuantC, kQuantC),
+                             noff = make_float2(-off, -off);
                 float2 rs[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) rs[i] = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const float2 x = __ffma2_rn(s[e], c12, nml);
+                    const float2 x = __fadd2_rn(__ffma2_rn(s[e], c12, qc), noff);
                     const float2 pe = make_float2(ex2(x.x), ex2(x.y));
                     rs[e & 3] = __fadd2_rn(rs[e & 3], pe);
                     w[e] = pack_bf16(pe.x, pe.y);
@@ -736,24 +743,25 @@ __global__ void __launch_bounds__(384, 1)
                 const float2 rs2 = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
                 rsum = rs2.x + rs2.y;
             };
-            // Lazy rescaling: the reference maximum m_run only moves when the
-            // row maximum exceeds it by more than 8 in log2 units, so P stays
-            // below 2^8 and O is rescaled rarely; O / l is unchanged.
+            // Lazy rescaling: the reference maximum m_run (an integer in log2
+            // units) only moves when the row maximum exceeds it by more than
+            // 8, so P stays below 2^8 and O is rescaled rarely (by an exact
+            // power of two); O / l is unchanged.
             float m_use = m_run;
             bool grow = false;
             if (m_run == -CUDART_INF_F) {
-                m_use = row_max();
+                m_use = ref_max(row_max() * kLog2e);
                 exp_pass(m_use);
             } else {
                 exp_pass(m_run);
-                const float rmx = row_max();
+                const float rmx = row_max() * kLog2e;
                 if (rmx > m_run + kLazyRescale) {
                     grow = true;
-                    m_use = rmx;
+                    m_use = ref_max(rmx);
                     exp_pass(m_use);
                 }
             }
-            const float alpha = grow ? ex2((m_run - m_use) * kLog2e) : 1.f;
+            const float alpha = grow ? exp2_int(m_run - m_use) : 1.f;
             // This half of P_j over the S columns this thread has already read
             // (PV_{j-2}, the last reader of the buffer, completed before S_j).
             tmem_st32(lane_base + sb * C::BN + kh, w);
@@ -832,10 +840,10 @@ __global__ void __launch_bounds__(384, 1)
             }
         }
         if (valid && partial && half == 0)
-            p.ws_lse[((size_t)split * p.T + t) * p.H + h] =
-                l_tot > 0.f ? m_run * kLog2e + __log2f(l_tot) : -CUDART_INF_F;
+            p.ws_lse[((size_t)split * p.T + t) * p.H + h] = l_tot > 0.f ? m_run + __log2f(l_tot) : -CUDART_INF_F;
         if (valid && !partial && half == 0 && p.lse)
-            p.lse[(size_t)t * p.lse_st + (size_t)h * p.lse_sh] = l_tot > 0.f ? m_run + logf(l_tot) : -CUDART_INF_F;
+            p.lse[(size_t)t * p.lse_st + (size_t)h * p.lse_sh] =
+                l_tot > 0.f ? (m_run + __log2f(l_tot)) * kLn2 : -CUDART_INF_F;
     }
 
     tc_fence_before();

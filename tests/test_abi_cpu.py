@@ -205,3 +205,35 @@ def test_cache_append_validates_before_device_work(what):
 def test_wait_timeout_self_test_rejects_out_of_range_limits(ms):
     L = _lib()
     assert L.lib.rel_attn_check_wait_timeout(ms, None) == 1
+
+
+@pytest.mark.parametrize("over", [
+    dict(num_splits=0), dict(rel_extent=-1), dict(rel_extent=9), dict(out="alias_q"),
+    dict(block_table=torch.zeros(3, 2, dtype=torch.int32)), dict(max_seqlen_q=-1),
+    dict(value_cache="strided"), dict(case=dict(head_dim=96)), dict(case=dict(block_size=8)),
+    dict(case=dict(num_heads=6, num_kv_heads=4)),
+], ids=["splits0", "rel_neg", "rel_shape", "alias", "table", "maxq", "v_strides", "d96", "bs8", "heads"])
+def test_noalloc_validates_like_the_allocating_entry_point(over):
+    """The allocation-free entry point shares the allocating one's validation:
+    the same status for every bad call, before any device work."""
+    L = _lib()
+    over = dict(over)
+    c = _cpu_case(**over.pop("case", {}))
+    if over.get("out") == "alias_q":
+        over["out"] = c.q
+    if over.get("value_cache") == "strided":
+        vc = torch.zeros(c.value_cache.shape[0], c.value_cache.shape[1], c.value_cache.shape[2],
+                         2 * c.value_cache.shape[3], dtype=torch.bfloat16)
+        over["value_cache"] = vc[..., :c.value_cache.shape[3]]
+    statuses = []
+    for fn in (L.rel_attn_paged_varlen, L.rel_attn_paged_varlen_noalloc):
+        args = dict(q=c.q, key_cache=c.key_cache, value_cache=c.value_cache, block_table=c.block_table,
+                    cache_seqlens=c.cache_seqlens, cu_seqlens_q=c.cu_seqlens_q, max_seqlen_q=c.max_seqlen_q,
+                    softmax_scale=c.softmax_scale, causal=c.causal, window_left=-1, window_right=-1,
+                    rel_extent=c.rel_extent, rel_logits=c.rel_logits, num_splits=1, out=torch.empty_like(c.q),
+                    stream=0)
+        args.update(over)
+        with pytest.raises(L.RelAttnError) as ei:
+            fn(**args)
+        statuses.append(ei.value.status)
+    assert statuses[0] == statuses[1] and statuses[0] in (1, 2), statuses

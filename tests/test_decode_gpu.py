@@ -43,7 +43,25 @@ def test_long_decode_matches_oracle(long_case, splits):
 
 def test_long_decode_split_equals_single(long_case):
     c, g, _ = long_case
-    assert_split_matches_single(c, g, 16)
+    d32 = assert_split_matches_single(c, g, 16)
+    print(f"long decode split 16 vs single, fp32 out: max |diff| {d32:.3e}")
+
+
+def test_decode_split_matches_single_concentrated_rows():
+    """Rows whose weight sits on a few keys (a large bias at a few distances):
+    the case where a P rounding that depended on the split partition would
+    move the output by most."""
+    c = make_case(seed=8, seqlens_q=[1, 4, 2], seqlens_k=[3000, 900, 2000], num_heads=16, num_kv_heads=2,
+                  head_dim=128, rel_extent=256)
+    rel = c.rel_logits.float()
+    rel[:, :, 3] += 12.0
+    rel[:, :, 200] += 9.0
+    c = c.with_(rel_logits=rel.to(torch.bfloat16))
+    g = to_dev(c)
+    for splits in (2, 5, 16):
+        d32 = assert_split_matches_single(c, g, splits)
+        print(f"decode concentrated rows, split {splits} vs single, fp32 out: max |diff| {d32:.3e}")
+    assert_close(run(c, g, num_splits=5), ref.forward(c), what="concentrated rows")
 
 
 def test_batched_decode_matches_oracle():

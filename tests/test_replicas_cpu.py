@@ -62,3 +62,29 @@ def test_reference_arm_runs_on_rank_zero_only():
     import bench
     args = argparse.Namespace(workload="no_such_workload", steps=1, warmup=3)
     assert bench.run_reference(args, rank=1, world=2) is None
+
+
+@pytest.mark.parametrize("workload", ["chunked_prefill", "mixed_window"])
+def test_multi_rank_run_refuses_prefill_workloads(workload):
+    """The prefill kernel loads K/V tiles with cluster multicast, which runs on
+    one GPU only: a multi-rank bench run of a prefill workload exits with a
+    clear message before touching a device or a process group."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, WORLD_SIZE="2", RANK="0", LOCAL_RANK="0", MASTER_ADDR="127.0.0.1", MASTER_PORT="1")
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--workload", workload, "--gpus", "2"],
+                       env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 2, (r.returncode, r.stderr[-2000:])
+    assert "1-GPU library" in r.stderr and "multicast" in r.stderr
+    assert r.stdout == ""
+
+
+def test_uses_prefill_follows_the_packed_row_rule():
+    import bench
+    from paged_attention_relative_gb300.workloads import make_case, tiny_mixed
+    assert not bench.uses_prefill(tiny_mixed(0))                      # 5 tokens x 2 heads per kv head
+    c = make_case(seed=0, seqlens_q=[17], seqlens_k=[40], num_heads=8, num_kv_heads=2, head_dim=64)
+    assert bench.uses_prefill(c)                                      # 17 x 4 = 68 rows > 64
+    c = make_case(seed=0, seqlens_q=[16], seqlens_k=[40], num_heads=8, num_kv_heads=2, head_dim=64)
+    assert not bench.uses_prefill(c)                                  # 64 rows
