@@ -42,6 +42,7 @@ if ROOT not in sys.path:
 METRIC = "decode HBM TB/s & % roofline; prefill TFLOP/s & % bf16 peak (1×GB300)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = {"decode": ["decode.cu", "common.cuh"], "prefill": ["prefill.cu", "common.cuh"],
+                  "prefill_pair": ["prefill_pair.cu", "common.cuh"],
                   "append": ["append.cu", "common.cuh"]}
 
 

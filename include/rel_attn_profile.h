@@ -19,7 +19,11 @@ typedef enum {
     REL_ATTN_KERNEL_NONE = 0,
     REL_ATTN_KERNEL_DECODE = 1,   /* split-KV decode kernel, <= 64 packed rows  */
     REL_ATTN_KERNEL_PREFILL = 2,  /* tcgen05 prefill kernel, 128-row tiles      */
-    REL_ATTN_KERNEL_APPEND = 3    /* paged KV-cache append (rel_attn_cache_append) */
+    REL_ATTN_KERNEL_APPEND = 3,   /* paged KV-cache append (rel_attn_cache_append) */
+    REL_ATTN_KERNEL_PREFILL_PAIR = 4  /* tcgen05 prefill kernel on CTA pairs (2-SM MMAs, cta_group::2);
+                                         head_dim 128 calls use it only when the environment variable
+                                         REL_ATTN_PREFILL_PAIR=1 is set (the one-CTA kernel is faster
+                                         there) */
 } rel_attn_kernel_kind;
 
 /* What the last rel_attn_paged_varlen call on this thread launched. */

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(HERE, "librel_attn.so")
 
 REL_ATTN_BF16, REL_ATTN_F32, REL_ATTN_I32 = 0, 1, 2
 STATUS = {0: "OK", 1: "INVALID_ARGUMENT", 2: "UNSUPPORTED", 3: "CUDA", 4: "OUT_OF_MEMORY", 5: "DEVICE_CHECK"}
-KERNELS = {0: "none", 1: "decode", 2: "prefill", 3: "append"}
+KERNELS = {0: "none", 1: "decode", 2: "prefill", 3: "append", 4: "prefill_pair"}
 
 # Every function the headers declare, with its ctypes signature.
 EXPORTS = ("rel_attn_paged_varlen", "rel_attn_paged_varlen_lse", "rel_attn_paged_varlen_noalloc", "rel_attn_num_splits",

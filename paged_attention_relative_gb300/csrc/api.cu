@@ -131,6 +131,23 @@ rel_attn_status make_cache_map(const rel_attn_tensor* t, CUtensorMap* map, const
     return REL_ATTN_OK;
 }
 
+// q (T, H, D) as a 3-D TMA tensor, innermost first: (D, H, T), box (64 dims,
+// G heads, 128 / G tokens) = one 64-dim block of a GQA-packed query tile,
+// 128-byte swizzle.
+rel_attn_status make_q_map(const rel_attn_tensor* t, int G, CUtensorMap* map) {
+    auto enc = encode_fn();
+    if (!enc) return fail(REL_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[3] = {(cuuint64_t)t->shape[2], (cuuint64_t)t->shape[1], (cuuint64_t)t->shape[0]};
+    cuuint64_t strides[2] = {(cuuint64_t)t->stride[1] * 2, (cuuint64_t)t->stride[0] * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(128 / G)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, t->data, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(REL_ATTN_ERR_UNSUPPORTED, "q: TMA descriptor rejected (CUresult %d)", (int)r);
+    return REL_ATTN_OK;
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 rel_attn_status check_tensor(const rel_attn_tensor* t, const char* name, int dtype, int ndim) {
@@ -195,6 +212,14 @@ uint64_t wait_timeout_ns() {
 
 bool check_enabled() {
     const char* s = std::getenv("REL_ATTN_CHECK");
+    return s && s[0] == '1';
+}
+
+// REL_ATTN_PREFILL_PAIR=1 sends head_dim-128 prefill calls with TMA-staged
+// or no bias to the CTA-pair kernel instead of the one-CTA kernel (both
+// compute the same attention; the one-CTA kernel is faster there).
+bool prefill_pair_requested() {
+    const char* s = std::getenv("REL_ATTN_PREFILL_PAIR");
     return s && s[0] == '1';
 }
 
@@ -511,8 +536,11 @@ rel_attn_status paged_varlen(
     p.timeout_ns = wait_timeout_ns();
     p.err = dev->err;
 
-    CUtensorMap maps[3];
+    CUtensorMap maps[4];
     std::memset(maps, 0, sizeof maps);
+    // The CTA-pair kernel (2-SM MMAs) on request for head_dim 128 with
+    // TMA-staged or no bias.
+    const bool pair = prefill && D == 128 && (rel_extent == 0 || p.vec_bias) && prefill_pair_requested();
     if (prefill) {
         if ((st = make_cache_map(key_cache, &maps[0], "key_cache"))) return st;
         if ((st = make_cache_map(value_cache, &maps[1], "value_cache"))) return st;
@@ -524,6 +552,7 @@ rel_attn_status paged_varlen(
             if (tpt % d == 0) ts = d;
         p.bias_ts = ts;
         if (p.vec_bias && (st = make_rel_map(rel_logits, (int)G, ts, &maps[2]))) return st;
+        if (pair && (st = make_q_map(q, (int)G, &maps[3]))) return st;
     }
 
     p.num_splits = (int32_t)splits;
@@ -548,11 +577,13 @@ rel_attn_status paged_varlen(
         p.ws_lse = p.ws_o + (size_t)splits * T * H * D;
     }
 
-    LaunchShape shape = prefill ? prefill_shape(p) : decode_shape(p, dev->sms);
+    LaunchShape shape = pair ? prefill_pair_shape(p) : prefill ? prefill_shape(p) : decode_shape(p, dev->sms);
     p.nstage = shape.nstage;
     p.nprod = shape.nprod;
     if (t_ev_begin) cudaEventRecord(t_ev_begin, stream);
-    cudaError_t e = prefill ? launch_prefill(p, maps, shape, stream) : launch_decode(p, shape, stream);
+    cudaError_t e = pair      ? launch_prefill_pair(p, maps, shape, stream)
+                    : prefill ? launch_prefill(p, maps, shape, stream)
+                              : launch_decode(p, shape, stream);
     if (t_ev_end) cudaEventRecord(t_ev_end, stream);
     int launches = 1;
     if (e == cudaSuccess && splits > 1) {
@@ -563,7 +594,7 @@ rel_attn_status paged_varlen(
         cudaError_t e2 = cudaFreeAsync(ws, stream);
         if (e == cudaSuccess) e = e2;
     }
-    t_launch.kernel = prefill ? REL_ATTN_KERNEL_PREFILL : REL_ATTN_KERNEL_DECODE;
+    t_launch.kernel = pair ? REL_ATTN_KERNEL_PREFILL_PAIR : prefill ? REL_ATTN_KERNEL_PREFILL : REL_ATTN_KERNEL_DECODE;
     t_launch.num_splits = (int32_t)splits;
     t_launch.grid[0] = (int32_t)shape.grid.x;
     t_launch.grid[1] = (int32_t)shape.grid.y;

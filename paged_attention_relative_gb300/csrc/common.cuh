@@ -233,6 +233,105 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return r;
 }
 
+// ---------------------------------------------------------------- CTA pairs
+
+// Address of the same shared-memory location in cluster CTA `rank`
+// (shared::cluster window).
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Arrive on an mbarrier given by its shared::cluster address (this CTA's or
+// the peer's), releasing this thread's prior writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Add `bytes` to the expected transaction count of the current phase of an
+// mbarrier given by its shared::cluster address.
+__device__ __forceinline__ void mbar_expect_tx_cluster(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cluster.shared::cluster.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// mbar_wait for barriers that the peer CTA arrives on (acquire at cluster scope).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint64_t timeout_ns, int site,
+                                                  int* err) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const long long budget = (long long)timeout_ns * 4;
+    const long long t0 = clock64();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (clock64() - t0 > budget) {
+            atomicCAS(err, 0, site);
+            return false;
+        }
+    }
+}
+
+// 4-D TMA load issued by either CTA of a pair whose completion is signalled
+// on an mbarrier that may live in the peer CTA (shared::cluster address).
+__device__ __forceinline__ void tma_load_4d_pair(void* dst, const void* desc, uint32_t bar, int c0, int c1, int c2,
+                                                 int c3, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const void* desc, uint32_t bar, int c0, int c1, int c2,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+        : "memory");
+}
+
+// 2-SM MMAs (cta_group::2): issued by one thread of the pair's even CTA; the
+// M = 256 rows are the two CTAs' 128 TMEM lanes at the same column, and the
+// B operand is split by N, each CTA holding its half at the same shared
+// address.  A from shared memory (ss) or from TMEM (ts).
+template <int ACC>
+__device__ __forceinline__ void umma2_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+    asm volatile("tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, %4;" ::"r"(d_tmem), "l"(a_desc),
+                 "l"(b_desc), "r"(idesc), "n"(ACC)
+                 : "memory");
+}
+
+template <int ACC>
+__device__ __forceinline__ void umma2_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc) {
+    asm volatile("tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, %4;" ::"r"(d_tmem), "r"(a_tmem),
+                 "l"(b_desc), "r"(idesc), "n"(ACC)
+                 : "memory");
+}
+
+// Arrive once on bar in both CTAs of the pair when every 2-SM MMA this
+// thread issued so far has completed.
+__device__ __forceinline__ void umma2_commit_both(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"((uint16_t)3)
+        : "memory");
+}
+
 // ---------------------------------------------------------------- cp.async
 
 // 16-byte global->shared copy through L2 only; src_bytes < 16 zero-fills the

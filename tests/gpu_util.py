@@ -10,6 +10,19 @@ TOL_SPLIT = 1e-3  # split vs one-split bound on the bf16 outputs
 FIELDS = ("q", "key_cache", "value_cache", "block_table", "cache_seqlens", "cu_seqlens_q", "rel_logits")
 
 
+def expected_prefill_kernel(c):
+    """The prefill kernel the library picks for a case above 64 packed rows:
+    the one-CTA kernel, or the CTA-pair kernel when REL_ATTN_PREFILL_PAIR=1
+    asks for it on head_dim 128 with TMA-staged bf16 rel_logits (R a multiple
+    of 8) or no bias."""
+    import os
+    D, R = c.q.shape[2], c.rel_extent
+    staged = R == 0 or (c.rel_logits.dtype == torch.bfloat16 and R % 8 == 0)
+    if D == 128 and staged and os.environ.get("REL_ATTN_PREFILL_PAIR", "") == "1":
+        return "prefill_pair"
+    return "prefill"
+
+
 def to_dev(c, dev="cuda"):
     return {k: getattr(c, k).to(dev) for k in FIELDS}
 

@@ -17,9 +17,11 @@ def _call(pa, c, g, out, max_seqlen_q, splits):
                              c.window_right, c.rel_extent, g["rel_logits"], splits, out=out)
 
 
-@pytest.mark.parametrize("kind", ["decode", "prefill"])
-def test_captured_call_replays_with_new_cache_lengths(kind):
+@pytest.mark.parametrize("kind", ["decode", "prefill", "prefill_pair"])
+def test_captured_call_replays_with_new_cache_lengths(kind, monkeypatch):
     import paged_attention_relative_gb300 as pa
+    if kind == "prefill_pair":
+        monkeypatch.setenv("REL_ATTN_PREFILL_PAIR", "1")
     if kind == "decode":
         c = make_case(seed=21, seqlens_q=[1, 1, 1], seqlens_k=[700, 1300, 260], num_heads=8, num_kv_heads=2,
                       head_dim=128, rel_extent=64)

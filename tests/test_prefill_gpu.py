@@ -11,7 +11,19 @@ import torch
 
 from oracle import reference as ref
 from paged_attention_relative_gb300.workloads import chunked_prefill, make_case, mixed_window
-from tests.gpu_util import assert_close, assert_no_device_error, assert_split_matches_single, run, to_dev
+from tests.gpu_util import (assert_close, assert_no_device_error, assert_split_matches_single,
+                            expected_prefill_kernel, run, to_dev)
+
+
+@pytest.fixture(params=["1cta", "pair"])
+def prefill_kernel(request, monkeypatch):
+    """Run a test on the one-CTA kernel (the default) and on the CTA-pair
+    kernel (REL_ATTN_PREFILL_PAIR=1)."""
+    if request.param == "pair":
+        monkeypatch.setenv("REL_ATTN_PREFILL_PAIR", "1")
+    else:
+        monkeypatch.delenv("REL_ATTN_PREFILL_PAIR", raising=False)
+    return request.param
 
 pytestmark = pytest.mark.gpu
 
@@ -59,19 +71,19 @@ SMALL = [
 
 @pytest.mark.parametrize("cfg", SMALL, ids=[c["name"] for c in SMALL])
 @pytest.mark.parametrize("splits", [1, 3])
-def test_prefill_small_cases_match_oracle(cfg, splits):
+def test_prefill_small_cases_match_oracle(cfg, splits, prefill_kernel):
     import paged_attention_relative_gb300 as pa
     kw = dict(cfg)
     name = kw.pop("name")
     kw.setdefault("rel_extent", 16)
     c = make_case(seed=(sum(map(ord, name)) % 997), **kw)
     got = run(c, num_splits=splits)
-    assert pa.last_launch()["kernel"] == "prefill"
+    assert pa.last_launch()["kernel"] == expected_prefill_kernel(c)
     assert_close(got, ref.forward(c), what=f"{name} splits={splits}")
     assert_no_device_error()
 
 
-def test_prefill_split_matches_single_fp32():
+def test_prefill_split_matches_single_fp32(prefill_kernel):
     c = make_case(seed=3, seqlens_q=[64, 40], seqlens_k=[900, 600], num_heads=8, num_kv_heads=2, head_dim=128,
                   rel_extent=200)
     g = to_dev(c)
@@ -83,7 +95,7 @@ def test_prefill_split_matches_single_fp32():
     assert_close(a, ref.forward(c), what="fp32 out")
 
 
-def test_prefill_split_matches_single_concentrated_rows():
+def test_prefill_split_matches_single_concentrated_rows(prefill_kernel):
     """Rows whose weight sits on a few keys (a large bias at a few distances):
     a bf16 rounding of P that depended on the split would show here first."""
     c = make_case(seed=4, seqlens_q=[70, 130], seqlens_k=[700, 1000], num_heads=8, num_kv_heads=2,
@@ -99,7 +111,7 @@ def test_prefill_split_matches_single_concentrated_rows():
     assert_close(run(c, g, num_splits=3), ref.forward(c), what="concentrated rows")
 
 
-def test_prefill_stale_page_tail_does_not_leak():
+def test_prefill_stale_page_tail_does_not_leak(prefill_kernel):
     c = make_case(seed=5, seqlens_q=[70], seqlens_k=[101], num_heads=4, num_kv_heads=2, head_dim=128,
                   rel_extent=16)
     k = c.key_cache.clone()
@@ -133,7 +145,7 @@ def test_chunked_prefill_every_output_matches_oracle(chunked_full, splits):
     import paged_attention_relative_gb300 as pa
     c, g, want = chunked_full
     got = run(c, g, num_splits=splits)
-    assert pa.last_launch()["kernel"] == "prefill"
+    assert pa.last_launch()["kernel"] == expected_prefill_kernel(c)
     assert pa.last_launch()["num_splits"] == splits
     _assert_full(got, want, f"chunked prefill splits={splits}")
     assert_no_device_error()
@@ -151,12 +163,12 @@ def test_mixed_window_every_output_matches_oracle():
     import paged_attention_relative_gb300 as pa
     c = mixed_window(0)
     got = run(c)
-    assert pa.last_launch()["kernel"] == "prefill"
+    assert pa.last_launch()["kernel"] == expected_prefill_kernel(c)
     _assert_full(got, ref.forward(c), "mixed window")
     assert_no_device_error()
 
 
-def test_prefill_batch_above_compact_limit():
+def test_prefill_batch_above_compact_limit(prefill_kernel):
     """More than 256 requests: every request gets max_seqlen_q's query tiles
     (empty clusters leave at once) instead of the compact cluster list."""
     import paged_attention_relative_gb300 as pa
@@ -167,21 +179,22 @@ def test_prefill_batch_above_compact_limit():
     c = make_case(seed=12, seqlens_q=sq.tolist(), seqlens_k=sk.tolist(), num_heads=8, num_kv_heads=2,
                   head_dim=64, rel_extent=16)
     got = run(c)
-    assert pa.last_launch()["kernel"] == "prefill"
+    assert pa.last_launch()["kernel"] == expected_prefill_kernel(c)
     assert pa.last_launch()["grid"][2] == 300
     assert_close(got, ref.forward(c), what="300 requests")
     assert_no_device_error()
 
 
-def test_prefill_compact_grid_with_inflated_max_seqlen_q():
+def test_prefill_compact_grid_with_inflated_max_seqlen_q(prefill_kernel):
     """max_seqlen_q far above the longest query: the compact launch is bounded
-    by the rows (T / 64 pairs plus one per request) and still covers every pair."""
+    by the rows (T / 64 pairs of 32-token tiles plus one per request) and
+    still covers every pair."""
     import paged_attention_relative_gb300 as pa
     c = make_case(seed=13, seqlens_q=[1, 130, 0, 65, 7], seqlens_k=[300, 400, 10, 65, 900], num_heads=8,
                   num_kv_heads=2, head_dim=128, rel_extent=40)
     got = run(c, max_seqlen_q=8 * c.max_seqlen_q, num_splits=2)
     info = pa.last_launch()
-    assert info["kernel"] == "prefill"
+    assert info["kernel"] == expected_prefill_kernel(c)
     T = c.q.shape[0]
     assert info["grid"][0] == 2 * ((T + 63) // 64 + 5)
     assert_close(got, ref.forward(c), what="inflated max_seqlen_q")
@@ -189,7 +202,7 @@ def test_prefill_compact_grid_with_inflated_max_seqlen_q():
 
 
 @pytest.mark.parametrize("splits", [1, 3])
-def test_prefill_strided_q_and_out_with_guard(splits):
+def test_prefill_strided_q_and_out_with_guard(splits, prefill_kernel):
     """q as a view into a packed (T, H + 2 Hk, D) projection, out as a view of a
     wider buffer: results match and nothing outside the out view is written."""
     c = make_case(seed=61, seqlens_q=[70, 33], seqlens_k=[300, 120], num_heads=8, num_kv_heads=2, head_dim=128,
