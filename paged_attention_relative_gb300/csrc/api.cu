@@ -415,7 +415,8 @@ rel_attn_status paged_varlen(
     }
     if (q->stride[2] != 1 || out->stride[2] != 1 || key_cache->stride[3] != 1 || value_cache->stride[3] != 1)
         return fail(REL_ATTN_ERR_INVALID_ARGUMENT, "the head_dim axis must be contiguous");
-    if (D != 64 && D != 128) return fail(REL_ATTN_ERR_UNSUPPORTED, "head_dim %lld unsupported (64 or 128)", (long long)D);
+    if (D != 64 && D != 128 && D != 256)
+        return fail(REL_ATTN_ERR_UNSUPPORTED, "head_dim %lld unsupported (64, 128 or 256)", (long long)D);
     if (BS <= 0 || BS % 16 != 0)
         return fail(REL_ATTN_ERR_UNSUPPORTED, "block_size %lld unsupported (a multiple of 16)", (long long)BS);
     if (H / Hk > 128) return fail(REL_ATTN_ERR_UNSUPPORTED, "more than 128 query heads per kv head");
@@ -538,9 +539,10 @@ rel_attn_status paged_varlen(
 
     CUtensorMap maps[4];
     std::memset(maps, 0, sizeof maps);
-    // The CTA-pair kernel (2-SM MMAs) on request for head_dim 128 with
-    // TMA-staged or no bias.
-    const bool pair = prefill && D == 128 && (rel_extent == 0 || p.vec_bias) && prefill_pair_requested();
+    // The CTA-pair kernel (2-SM MMAs): head_dim 256 always (only it fits
+    // that head size), head_dim 128 with TMA-staged or no bias on request.
+    const bool pair =
+        prefill && (D == 256 || (D == 128 && (rel_extent == 0 || p.vec_bias) && prefill_pair_requested()));
     if (prefill) {
         if ((st = make_cache_map(key_cache, &maps[0], "key_cache"))) return st;
         if ((st = make_cache_map(value_cache, &maps[1], "value_cache"))) return st;

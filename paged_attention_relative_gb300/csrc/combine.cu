@@ -2,7 +2,7 @@
 // M = max_s lse_s, where o_s is split s's normalised partial output and lse_s
 // its log2-sum-exp; a row whose every split is empty (all lse = -inf) gets 0.
 // When requested, the row's natural-log sum-exp (M + log2 sum) * ln 2 goes to lse.
-// One warp per (token, head) row, D/32 contiguous dims per lane.
+// One warp per (token, head) row, D/32 contiguous dims per lane (D = 64, 128, 256).
 //
 // The split count is the num_splits argument of inkling_fa4_rel_attention
 // (vLLM API docs, fa4_rel_attention); the merge itself is the standard
@@ -68,7 +68,18 @@ __global__ void __launch_bounds__(256) combine_kernel(const AttnParams p) {
                 const float w = __shfl_sync(0xffffffffu, w_l, j);
                 L += w;
                 const float* src = base + (size_t)(s0 + j) * split_stride;
-                if constexpr (V == 4) {
+                if constexpr (V == 8) {
+                    const float4 v = *reinterpret_cast<const float4*>(src);
+                    const float4 u = *reinterpret_cast<const float4*>(src + 4);
+                    acc[0] = fmaf(w, v.x, acc[0]);
+                    acc[1] = fmaf(w, v.y, acc[1]);
+                    acc[2] = fmaf(w, v.z, acc[2]);
+                    acc[3] = fmaf(w, v.w, acc[3]);
+                    acc[4] = fmaf(w, u.x, acc[4]);
+                    acc[5] = fmaf(w, u.y, acc[5]);
+                    acc[6] = fmaf(w, u.z, acc[6]);
+                    acc[7] = fmaf(w, u.w, acc[7]);
+                } else if constexpr (V == 4) {
                     const float4 v = *reinterpret_cast<const float4*>(src);
                     acc[0] = fmaf(w, v.x, acc[0]);
                     acc[1] = fmaf(w, v.y, acc[1]);
@@ -91,14 +102,25 @@ __global__ void __launch_bounds__(256) combine_kernel(const AttnParams p) {
     const size_t oo = (size_t)t * p.o_st + (size_t)h * p.o_sh + lane * V;
     if (p.out_f32) {
         float* dst = reinterpret_cast<float*>(p.out) + oo;
-        if constexpr (V == 4)
+        if constexpr (V == 8) {
             *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        else
+            *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        } else if constexpr (V == 4) {
+            *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        } else {
             *reinterpret_cast<float2*>(dst) = make_float2(acc[0], acc[1]);
+        }
         return;
     }
     uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + oo;
-    if constexpr (V == 4) {
+    if constexpr (V == 8) {
+        uint4 pk;
+        pk.x = pack_bf16(acc[0], acc[1]);
+        pk.y = pack_bf16(acc[2], acc[3]);
+        pk.z = pack_bf16(acc[4], acc[5]);
+        pk.w = pack_bf16(acc[6], acc[7]);
+        *reinterpret_cast<uint4*>(dst) = pk;
+    } else if constexpr (V == 4) {
         uint2 pk;
         pk.x = pack_bf16(acc[0], acc[1]);
         pk.y = pack_bf16(acc[2], acc[3]);
@@ -123,7 +145,9 @@ cudaError_t launch_combine(const AttnParams& p, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e;
-    if (p.D == 128)
+    if (p.D == 256)
+        e = cudaLaunchKernelEx(&cfg, combine_kernel<256>, p);
+    else if (p.D == 128)
         e = cudaLaunchKernelEx(&cfg, combine_kernel<128>, p);
     else if (p.D == 64)
         e = cudaLaunchKernelEx(&cfg, combine_kernel<64>, p);

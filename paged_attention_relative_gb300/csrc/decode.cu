@@ -8,8 +8,9 @@
 // page slice, keys past the visible range zero-filled) into a ring of NSTAGE
 // slots whose rows are padded by 16 bytes, so the ldmatrix reads are
 // conflict-free; completion is signalled on the slot's mbarrier by
-// cp.async.mbarrier.arrive.  KSL x MT consumer warps each take one 16-key
-// slice of a stage and one 16-row tile: QK^T and PV on bf16 mma.sync with
+// cp.async.mbarrier.arrive.  KSL x MT consumer warps (x 2 with head_dim 256,
+// one per dim half, adding their partial scores through shared memory) each
+// take one 16-key slice of a stage and one 16-row tile: QK^T and PV on bf16 mma.sync with
 // fp32 accumulation, the scale, the sheared relative bias and the mask per
 // element (skipped for slices wholly visible and outside the bias band), and
 // an fp32 online softmax in base 2; then they release the slot.  The
@@ -36,7 +37,13 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D, int MT, int KSL>
 struct DecodeCfg {
-    static constexpr int kConsumers = MT * KSL;
+    // head_dim 256: each 16-key slice goes to a pair of warps, each owning
+    // half of the dims (a 16-row fragment of 256 fp32 accumulators per lane
+    // would not fit in registers); they add their partial scores through
+    // shared memory, so both hold the same softmax state.
+    static constexpr int DS = D == 256 ? 2 : 1;       // dim halves per slice
+    static constexpr int DW = D / DS;                 // dims one warp owns
+    static constexpr int kConsumers = MT * KSL * DS;
     static constexpr int kMaxProducers = 4;
     static constexpr int kMaxThreads = (kConsumers + kMaxProducers) * 32;
     static constexpr int kStageKeys = 16 * KSL;
@@ -50,6 +57,10 @@ struct DecodeCfg {
     static constexpr int kRedStride = D + 4;         // floats per row in the merge area
     static constexpr int kRedBytes = KSL * MT * 16 * (kRedStride + 2) * 4;
     static constexpr int kMaxStages = 12;
+    // Partial-score exchange (DS == 2): per warp pair, two tile-parity
+    // buffers of 32 lanes x 8 floats per warp, and two mbarriers.
+    static constexpr int kPairs = DS == 2 ? MT * KSL : 0;
+    static constexpr int kXchBytes = kPairs * 2 * 2 * 32 * 8 * 4;
 };
 
 constexpr int kRankMax = 256;
@@ -68,7 +79,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, KSL>::kMaxThreads) decode_ker
                                                                              : (size_t)C::kRedBytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + body);
     uint64_t* empty = full + C::kMaxStages;
-    int* abort_flag = reinterpret_cast<int*>(empty + C::kMaxStages);
+    uint64_t* xbar = empty + C::kMaxStages;  // [pair][tile parity], C::kPairs * 2
+    int* abort_flag = reinterpret_cast<int*>(xbar + 2 * C::kPairs);
+    float* xch = reinterpret_cast<float*>(abort_flag + 4);  // [pair][parity][dim half][32 lanes][8]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x, g = blockIdx.y;
@@ -124,6 +137,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, KSL>::kMaxThreads) decode_ker
             mbar_init(&full[i], 32 * p.nprod);     // one arrival per producer lane
             mbar_init(&empty[i], C::kConsumers);  // one arrival per consumer warp
         }
+        for (int i = 0; i < 2 * C::kPairs; ++i) mbar_init(&xbar[i], 2);  // both warps of the pair
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -182,7 +196,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, KSL>::kMaxThreads) decode_ker
     }
 
     // ---------------------------------------------------------------- consumers
-    const int mt = warp % MT, ks = warp / MT;  // row tile, 16-key slice of each stage
+    // row tile, 16-key slice of each stage, dim half (head_dim 256)
+    const int mt = warp % MT, ks = (warp / MT) % KSL, dh = warp / (MT * KSL);
 
     // ------------------------------------------------------------- rows
     const int gq = lane >> 2, tig = lane & 3;
@@ -202,26 +217,27 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, KSL>::kMaxThreads) decode_ker
     // Extreme key positions over the CTA's valid rows (rows are token-major).
     const int pos_lo = off, pos_hi = (n_rows - 1) / G + off;
 
-    // Q fragments (A operand, rows x dims), loaded once.
-    uint32_t qf[D / 16][4];
+    // Q fragments (A operand, rows x this warp's dims), loaded once.
+    uint32_t qf[C::DW / 16][4];
     {
         const uint16_t* qb = reinterpret_cast<const uint16_t*>(p.q);
         const uint32_t* rowp0 =
             reinterpret_cast<const uint32_t*>(qb + (size_t)(q0 + qi0) * p.q_st + (size_t)h0 * p.q_sh);
         const uint32_t* rowp1 =
             reinterpret_cast<const uint32_t*>(qb + (size_t)(q0 + qi1) * p.q_st + (size_t)h1 * p.q_sh);
+        const int w0 = dh * (C::DW / 2);  // first 32-bit word of this warp's dims
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            qf[kk][0] = valid0 ? __ldg(rowp0 + kk * 8 + tig) : 0u;
-            qf[kk][1] = valid1 ? __ldg(rowp1 + kk * 8 + tig) : 0u;
-            qf[kk][2] = valid0 ? __ldg(rowp0 + kk * 8 + 4 + tig) : 0u;
-            qf[kk][3] = valid1 ? __ldg(rowp1 + kk * 8 + 4 + tig) : 0u;
+        for (int kk = 0; kk < C::DW / 16; ++kk) {
+            qf[kk][0] = valid0 ? __ldg(rowp0 + w0 + kk * 8 + tig) : 0u;
+            qf[kk][1] = valid1 ? __ldg(rowp1 + w0 + kk * 8 + tig) : 0u;
+            qf[kk][2] = valid0 ? __ldg(rowp0 + w0 + kk * 8 + 4 + tig) : 0u;
+            qf[kk][3] = valid1 ? __ldg(rowp1 + w0 + kk * 8 + 4 + tig) : 0u;
         }
     }
 
-    float o[D / 8][4];
+    float o[C::DW / 8][4];
 #pragma unroll
-    for (int a = 0; a < D / 8; ++a) o[a][0] = o[a][1] = o[a][2] = o[a][3] = 0.f;
+    for (int a = 0; a < C::DW / 8; ++a) o[a][0] = o[a][1] = o[a][2] = o[a][3] = 0.f;
     // m_run: reference maximum of each row, an integer in log2 units (the
     // ceiling of the running maximum; see kQuantC: weights then do not
     // depend on the split partition).  O and l are rescaled, by an exact
@@ -255,9 +271,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, KSL>::kMaxThreads) decode_ker
         {
             const int krow = (lane >> 4) * 8 + (lane & 7);
             const int csel = (lane >> 3) & 1;
-            const uint32_t kb = smem_u32(kbuf) + krow * C::kRowBytes + csel * 16;
+            const uint32_t kb = smem_u32(kbuf) + krow * C::kRowBytes + csel * 16 + dh * C::DW * 2;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
+            for (int kk = 0; kk < C::DW / 16; ++kk) {
                 const uint32_t addr = kb + kk * 32;
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4(addr, b0, b1, b2, b3);
@@ -269,6 +285,34 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, KSL>::kMaxThreads) decode_ker
                     mma_bf16_16816(sacc[1], qf[kk], b2, b3);
                 }
             }
+        }
+
+        if constexpr (C::DS == 2) {
+            // Add the partner warp's partial scores (its half of the dims).
+            // Both warps form partial + partial in IEEE arithmetic, which is
+            // commutative, so they hold bit-identical scores.
+            const int pair = mt + MT * ks, par = it & 1;
+            float* mine = xch + (((pair * 2 + par) * 2 + dh) * 32 + lane) * 8;
+            const float* theirs = xch + (((pair * 2 + par) * 2 + (dh ^ 1)) * 32 + lane) * 8;
+#pragma unroll
+            for (int a = 0; a < 2; ++a)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) mine[a * 4 + e] = sacc[a][e] + sacc2[a][e];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&xbar[pair * 2 + par]);
+            const bool xok = mbar_wait(&xbar[pair * 2 + par], (uint32_t)((it >> 1) & 1), p.timeout_ns,
+                                       kSiteDecodeFull, p.err);
+            if (!__all_sync(0xffffffffu, xok)) {
+                if (lane == 0) *abort_flag = 1;
+                break;
+            }
+#pragma unroll
+            for (int a = 0; a < 2; ++a)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    sacc[a][e] = mine[a * 4 + e] + theirs[a * 4 + e];
+                    sacc2[a][e] = 0.f;
+                }
         }
 
         // Scale, sheared bias, mask.  Warp-uniform fast path: every key of the
@@ -353,9 +397,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, KSL>::kMaxThreads) decode_ker
         {
             const int vrow = ((lane >> 3) & 1) * 8 + (lane & 7);
             const int csel = lane >> 4;
-            const uint32_t vb = smem_u32(vbuf) + vrow * C::kRowBytes + csel * 16;
+            const uint32_t vb = smem_u32(vbuf) + vrow * C::kRowBytes + csel * 16 + dh * C::DW * 2;
 #pragma unroll
-            for (int n2 = 0; n2 < D / 16; ++n2) {
+            for (int n2 = 0; n2 < C::DW / 16; ++n2) {
                 const uint32_t addr = vb + n2 * 32;
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4_t(addr, b0, b1, b2, b3);
@@ -385,11 +429,11 @@ __global__ void __launch_bounds__(DecodeCfg<D, MT, KSL>::kMaxThreads) decode_ker
 #pragma unroll
     for (int rsel = 0; rsel < 2; ++rsel) {
         const int r = rsel ? r1 : r0;
-        float* dst = red_o + ((size_t)ks * rows_cta + r) * C::kRedStride;
+        float* dst = red_o + ((size_t)ks * rows_cta + r) * C::kRedStride + dh * C::DW;
 #pragma unroll
-        for (int a = 0; a < D / 8; ++a)
+        for (int a = 0; a < C::DW / 8; ++a)
             *reinterpret_cast<float2*>(dst + a * 8 + 2 * tig) = make_float2(o[a][2 * rsel], o[a][2 * rsel + 1]);
-        if (tig == 0) {
+        if (tig == 0 && dh == 0) {
             red_m[ks * rows_cta + r] = m_run[rsel];
             red_l[ks * rows_cta + r] = l_run[rsel];
         }
@@ -452,7 +496,7 @@ int decode_smem_bytes(int nst) {
     using C = DecodeCfg<D, MT, KSL>;
     int body = nst * C::kStageBytes;
     if (body < C::kRedBytes) body = C::kRedBytes;
-    return 128 + body + 2 * C::kMaxStages * 8 + 16;
+    return 128 + body + 2 * C::kMaxStages * 8 + 2 * C::kPairs * 8 + 16 + C::kXchBytes;
 }
 
 template <int D, int MT, int KSL>
@@ -461,7 +505,7 @@ int pick_stages(int ctas, int num_sms) {
     // One CTA per SM when the grid fits in one wave or the CTA has eight
     // consumer warps, else two per SM; the ring takes what shared memory
     // allows so the producers run far ahead.
-    const int budget = (ctas <= num_sms || KSL == 8) ? 224 * 1024 : 111 * 1024;
+    const int budget = (ctas <= num_sms || C::kConsumers >= 8) ? 224 * 1024 : 111 * 1024;
     int n = (budget - 512) / C::kStageBytes;
     if (n > C::kMaxStages) n = C::kMaxStages;
     if (n < 2) n = 2;
@@ -480,29 +524,33 @@ cudaError_t launch_t(const AttnParams& p, const LaunchShape& s, cudaStream_t str
 }  // namespace
 
 // Tile shape: up to 16 packed rows use one 16-row MMA tile and 8 key groups
-// (8 warps); 17-32 rows use 2 row tiles x 4 groups, 33-64 rows 4 x 2.
+// (8 warps); 17-32 rows use 2 row tiles x 4 groups, 33-64 rows 4 x 2.  With
+// head_dim 256 each group takes a pair of warps (one per dim half), so the
+// groups halve: 4, 2 and 1.
 LaunchShape decode_shape(const AttnParams& p, int num_sms) {
     LaunchShape s;
     const int ctas = p.num_splits * p.Hk * p.B;
+    const int ds = p.D == 256 ? 2 : 1;
     if (p.max_rows <= 16) {
         s.mt = 1;
         // Eight consumer warps and four producers, one CTA per SM: one CTA
         // streams its (request, kv head) at close to an SM's share of HBM
         // bandwidth, and with the longest requests first the grid's tail is
         // the short ones.
-        s.ksl = 8;
+        s.ksl = 8 / ds;
     } else if (p.max_rows <= 32) {
         s.mt = 2;
-        s.ksl = 4;
+        s.ksl = 4 / ds;
     } else {
         s.mt = 4;
-        s.ksl = 2;
+        s.ksl = 2 / ds;
     }
     s.grid = dim3(p.num_splits, p.Hk, p.B);
     // Four producer warps next to the eight consumers: a single issuing warp
     // cannot keep enough 16-byte gathers in flight.
-    s.nprod = s.mt * s.ksl >= 8 ? 4 : 2;
-    s.block = (s.mt * s.ksl + s.nprod) * 32;
+    const int consumers = s.mt * s.ksl * ds;
+    s.nprod = consumers >= 8 ? 4 : 2;
+    s.block = (consumers + s.nprod) * 32;
 #define REL_ATTN_SHAPE(DD, M, K)                         \
     if (p.D == DD && s.mt == M && s.ksl == K) {         \
         s.nstage = pick_stages<DD, M, K>(ctas, num_sms); \
@@ -514,6 +562,9 @@ LaunchShape decode_shape(const AttnParams& p, int num_sms) {
     REL_ATTN_SHAPE(128, 1, 8)
     REL_ATTN_SHAPE(128, 2, 4)
     REL_ATTN_SHAPE(128, 4, 2)
+    REL_ATTN_SHAPE(256, 1, 4)
+    REL_ATTN_SHAPE(256, 2, 2)
+    REL_ATTN_SHAPE(256, 4, 1)
 #undef REL_ATTN_SHAPE
     return s;
 }
@@ -528,6 +579,9 @@ cudaError_t launch_decode(const AttnParams& p, const LaunchShape& s, cudaStream_
     REL_ATTN_LAUNCH(128, 1, 8)
     REL_ATTN_LAUNCH(128, 2, 4)
     REL_ATTN_LAUNCH(128, 4, 2)
+    REL_ATTN_LAUNCH(256, 1, 4)
+    REL_ATTN_LAUNCH(256, 2, 2)
+    REL_ATTN_LAUNCH(256, 4, 1)
 #undef REL_ATTN_LAUNCH
     return cudaErrorInvalidValue;
 }

@@ -1,5 +1,5 @@
 // Prefill / chunked-prefill kernel on CTA pairs: 2-SM tcgen05 MMAs
-// (cta_group::2), head_dim 128, rel_logits staged by TMA or no bias.
+// (cta_group::2), head_dim 128 or 256.
 //
 // One cluster of two CTAs per (pair of adjacent 128-row query tiles, kv
 // head, request, split).  Rows are GQA-packed token-major as in the other
@@ -8,9 +8,11 @@
 // (M = 256) covers both tiles, issued by a single thread of the even CTA.
 // The pair walks one sequence of 128-key tiles (the union of its tiles'
 // visible ranges, last tile first); each CTA stages half of every tile,
-// keys [64 r, 64 r + 64) of K (both 64-dim blocks) and dims [64 r, 64 r + 64)
-// of V (all 128 keys): the split of the B operand that the 2-SM MMA reads
-// from the two CTAs.  No TMA multicast: every box is loaded once, by the CTA
+// keys [64 r, 64 r + 64) of K (every 64-dim block) and dims
+// [D/2 r, D/2 r + D/2) of V (all 128 keys): the split of the B operand that
+// the 2-SM MMA reads from the two CTAs.  Halving K and V per CTA is what
+// makes head_dim 256 fit: O takes TMEM columns [256, 512) and the 64 KB
+// query tile, K and V halves and two bias windows stay within 227 KB.  No TMA multicast: every box is loaded once, by the CTA
 // that holds it, and signals the even CTA's barrier.  A CTA whose tile lies
 // past the request still takes part (its half of K/V, its softmax) and
 // writes nothing.
@@ -22,14 +24,15 @@
 // PV_j completed.
 //
 // Warp roles (384 threads per CTA):
-//   warp 0     the query tile (TMA, two boxes), then this CTA's half of every
-//              K tile into a 2-slot ring: 2 KB boxes (16 keys x 64 dims)
+//   warp 0     the query tile (TMA, one box per 64-dim block), then this CTA's
+//              half of every K tile into a ring (2 slots, 1 for head_dim
+//              256): 2 KB boxes (16 keys x 64 dims)
 //              straight from the paged cache, zero-filling cp.async for
 //              16-key groups only partly visible.
 //   warp 1     bias windows: for each band tile one TMA box per 8-token
-//              sub-box into one of three window buffers, once the softmax has
-//              released that buffer's previous fill.
-//   warp 2     this CTA's half of every V tile into a 2-slot ring.
+//              sub-box into one of three (head_dim 256: two) window buffers,
+//              once the softmax has released that buffer's previous fill.
+//   warp 2     this CTA's half of every V tile into a ring like K's.
 //   warp 3     TMEM (512 columns, allocated by the pair) and, in the even
 //              CTA, the MMA thread.
 //   warps 4-11 softmax as in the one-CTA kernel: thread (w, lane) owns keys
@@ -40,7 +43,7 @@
 //              lazily (see kQuantC), P into TMEM over the S columns already
 //              read, a rare rescale of O, the epilogue.
 //
-// TMEM columns: S_0 [0, 128), S_1 [128, 256), O [256, 384).  P_j lies in S
+// TMEM columns: S_0 [0, 128), S_1 [128, 256), O [256, 256 + D).  P_j lies in S
 // buffer j % 2: keys [64 h, 64 h + 64) in columns [64 h, 64 h + 32).
 // Every mbarrier wait is bounded; on timeout the kernel records the site in
 // the device error word and winds down.
@@ -60,20 +63,24 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazyRescale = 8.0f;  // log2 units
 
+template <int D_>
 struct PairCfg {
-    static constexpr int D = 128;
+    static constexpr int D = D_;
     static constexpr int BN = 128;                    // keys per tile
-    static constexpr int kQBytes = 2 * 128 * 128;     // the query tile: 2 dim blocks x 128 rows x 128 B
-    static constexpr int kKBytes = 2 * 64 * 128;      // this CTA's K half: 2 dim blocks x 64 keys x 128 B
-    static constexpr int kVBytes = 128 * 128;         // this CTA's V half: 128 keys x 64 dims
+    static constexpr int kDB = D / 64;                // 64-dim (128-byte) blocks
+    static constexpr int kVB = D / 128;               // 64-dim blocks of this CTA's V half
+    static constexpr int kQBytes = kDB * 128 * 128;   // the query tile: kDB blocks x 128 rows x 128 B
+    static constexpr int kKBytes = kDB * 64 * 128;    // this CTA's K half: kDB blocks x 64 keys x 128 B
+    static constexpr int kVBytes = kVB * 128 * 128;   // this CTA's V half: kVB blocks x 128 keys x 128 B
+    static constexpr int kRing = D == 128 ? 2 : 1;    // K and V ring slots
     static constexpr int kBiasW = 152;                // rel_logits values per staged row
     static constexpr int kBiasBytes = 128 * kBiasW * 2 + 16 * 128;
-    static constexpr int kBiasBufs = 3;
+    static constexpr int kBiasBufs = D == 128 ? 3 : 2;
     static constexpr int kXchBytes = 3 * 2 * 128 * 4;  // half-row maxima (2 tile buffers), half-row sums
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + kQBytes;
-    static constexpr int kOffV = kOffK + 2 * kKBytes;
-    static constexpr int kOffBias = kOffV + 2 * kVBytes;
+    static constexpr int kOffV = kOffK + kRing * kKBytes;
+    static constexpr int kOffBias = kOffV + kRing * kVBytes;
     static constexpr int kOffXch = kOffBias + kBiasBufs * kBiasBytes;
     static constexpr int kData = kOffXch + kXchBytes;
     static constexpr int kThreads = 384;
@@ -84,11 +91,11 @@ struct PairCfg {
 
 struct PairBars {
     uint64_t q_full;            // even CTA: both CTAs' query tiles have landed
-    uint64_t k_full[2];         // even CTA: K slot filled in both CTAs
-    uint64_t v_full[2];         // even CTA: V slot filled in both CTAs
+    uint64_t k_full[2];         // even CTA: K slot filled in both CTAs (one phase per fill)
+    uint64_t v_full[2];         // even CTA: V slot filled in both CTAs (one phase per fill)
     uint64_t p_full[2];         // even CTA: P in S buffer b written by both CTAs' softmax warps
-    uint64_t s_full[2];         // both: S_j of S buffer / K slot j % 2 computed (one phase per use)
-    uint64_t o_done[2];         // both: PV_j of V slot j % 2 completed (one phase per use)
+    uint64_t s_full[2];         // both: S_j of S buffer j % 2 computed (one phase per use)
+    uint64_t o_done[2];         // both: PV_j, j % 2, completed (one phase per use)
     uint64_t x_full[2];         // this CTA: per tile parity, every softmax warp published its half-row maxima
     uint64_t o_final;           // both: every MMA of the item completed
     uint64_t bias_full[3];      // this CTA: window buffer filled (one phase per fill)
@@ -143,11 +150,12 @@ __device__ __forceinline__ int2 compact_pair(const int32_t* cu, int B, int TPT, 
     return make_int2(-1, 0);
 }
 
+template <int D>
 __global__ void __launch_bounds__(384, 1)
     prefill_pair_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_rel,
                         const __grid_constant__ CUtensorMap tm_q) {
-    using C = PairCfg;
+    using C = PairCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem + C::kOffQ;
@@ -260,10 +268,10 @@ __global__ void __launch_bounds__(384, 1)
             // rows past G * TPT are zeroed once so that S stays finite there.
             const int q_rows = G * TPT;
             if (q_rows < 128) {
-                for (int i = lane; i < 2 * (128 - q_rows) * 8; i += 32) {
+                for (int i = lane; i < C::kDB * (128 - q_rows) * 8; i += 32) {
                     const int chunk = i & 7, row = q_rows + ((i >> 3) % (128 - q_rows));
                     const int db = (i >> 3) / (128 - q_rows);
-                    *reinterpret_cast<uint4*>(sQ + db * (C::kQBytes / 2) +
+                    *reinterpret_cast<uint4*>(sQ + db * (128 * 128) +
                                               sw128_offset((uint32_t)row, (uint32_t)chunk)) = make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
@@ -272,23 +280,29 @@ __global__ void __launch_bounds__(384, 1)
             if (lane == 0) {
                 const uint32_t qbar = mapa_shared(smem_u32(&bars->q_full), 0);
                 tma_prefetch_desc(&tm_q);
-                mbar_expect_tx_cluster(qbar, (uint32_t)(2 * q_rows * 128));
-                for (int db = 0; db < 2; ++db)
-                    tma_load_3d_pair(sQ + db * (C::kQBytes / 2), &tm_q, qbar, 64 * db, g * G, q0 + i0, pol_last);
+                mbar_expect_tx_cluster(qbar, (uint32_t)(C::kDB * q_rows * 128));
+                for (int db = 0; db < C::kDB; ++db)
+                    tma_load_3d_pair(sQ + db * (128 * 128), &tm_q, qbar, 64 * db, g * G, q0 + i0, pol_last);
                 mbar_arrive_cluster(qbar);
             }
             __syncwarp();
         }
         // 16-key groups of a tile this CTA stages: K groups 4 rank .. 4 rank + 3
-        // (both dim blocks), V groups 0 .. 7 (dim block `rank`).
+        // (every dim block; layout [dim block][64 keys][128 B]), V groups
+        // 0 .. 7 (dim blocks kVB rank .. kVB rank + kVB - 1; layout
+        // [dim block][128 keys][128 B]).
         const int g_first = is_v ? 0 : 4 * rank;
         const int n_groups = is_v ? 8 : 4;
+        const int n_db = is_v ? C::kVB : C::kDB;       // dim blocks per group this CTA stages
+        const int db_first = is_v ? C::kVB * rank : 0;
+        const int db_stride = is_v ? 128 * 128 : 64 * 128;  // bytes between dim blocks in a slot
         const int slot_bytes = is_v ? C::kVBytes : C::kKBytes;
         uint8_t* ring = is_v ? sV : sK;
         uint32_t full_bar[2];
         for (int i = 0; i < 2; ++i)
             full_bar[i] = mapa_shared(smem_u32(is_v ? &bars->v_full[i] : &bars->k_full[i]), 0);
-        // Ring slot k is free again once S (K) or PV (V) of the tile it held completed.
+        // The slot of tile jj is free again once S (K) or PV (V) of tile
+        // jj - kRing, the tile it held, has completed (barrier (jj - kRing) % 2).
         uint64_t* free_bar[2] = {is_v ? &bars->o_done[0] : &bars->s_full[0], is_v ? &bars->o_done[1] : &bars->s_full[1]};
         // At most one cp.async batch (the partial groups of a tile) is in
         // flight; it is retired (landed, proxy-fenced, one arrival with a
@@ -316,13 +330,14 @@ __global__ void __launch_bounds__(384, 1)
         };
         int win_cur = load_win(0), win_nxt = load_win(4);
         for (int jj = 0; jj < n_it; ++jj) {
-            const int slot = jj & 1;
-            if (jj >= 2) {
-                // Slot `slot` last held tile jj - 2 (use (jj - 2) / 2 of the slot).
-                const uint32_t par = (uint32_t)(((jj - 2) >> 1) & 1);
-                if (!mbar_try_wait(free_bar[slot], par)) {
+            const int slot = jj % C::kRing;
+            if (jj >= C::kRing) {
+                // The slot last held tile jj - kRing: use (jj - kRing) / 2 of barrier (jj - kRing) % 2.
+                const int prev = jj - C::kRing;
+                const uint32_t par = (uint32_t)((prev >> 1) & 1);
+                if (!mbar_try_wait(free_bar[prev & 1], par)) {
                     if (pend >= 0) retire(0);
-                    if (!mbar_wait(free_bar[slot], par, p.timeout_ns, kSitePrefillKEmpty, p.err)) bars->abort = 1;
+                    if (!mbar_wait(free_bar[prev & 1], par, p.timeout_ns, kSitePrefillKEmpty, p.err)) bars->abort = 1;
                 }
             }
             if (__any_sync(0xffffffffu, aborted(bars))) break;
@@ -338,25 +353,26 @@ __global__ void __launch_bounds__(384, 1)
                 if (jg >= lo && jg + 16 <= hi) full_mask |= 1u << i;
             }
             uint8_t* tile = ring + slot * slot_bytes;
-            const int boxes = __popc(full_mask) * (is_v ? 1 : 2);
-            if (lane == 0) mbar_expect_tx_cluster(full_bar[slot], (uint32_t)boxes * 2048u);
+            const int boxes = __popc(full_mask) * n_db;
+            if (lane == 0) mbar_expect_tx_cluster(full_bar[jj & 1], (uint32_t)boxes * 2048u);
             __syncwarp();
-            // TMA lanes 0-7: K lane -> (group lane / 2, dim block lane % 2),
-            // V lane -> group lane (dim block `rank`).
+            // TMA lanes: lane -> (local group lane / n_db, dim block lane % n_db),
+            // n_groups * n_db boxes (8 with head_dim 128, 16 with 256).
             {
-                const int li = is_v ? (lane & 7) : ((lane >> 1) & 3);
-                const int db = is_v ? rank : (lane & 1);
+                const int li = (lane / n_db) & (n_groups - 1);
+                const int dbl = lane % n_db;
                 const int pg = g_first + li;
                 const int blk = min(max(__shfl_sync(0xffffffffu, win_cur, wl + pg), 0), p.NB - 1);
-                if (lane < 8 && ((full_mask >> li) & 1)) {
-                    uint8_t* dst = is_v ? tile + pg * 2048 : tile + db * (C::kKBytes / 2) + li * 2048;
-                    tma_load_4d_pair(dst, tmap, full_bar[slot], 64 * db, g, (j0 + 16 * pg) % p.BS, blk, pol_last);
+                if (lane < n_groups * n_db && ((full_mask >> li) & 1)) {
+                    uint8_t* dst = tile + dbl * db_stride + (is_v ? pg : li) * 2048;
+                    tma_load_4d_pair(dst, tmap, full_bar[jj & 1], 64 * (db_first + dbl), g, (j0 + 16 * pg) % p.BS, blk,
+                                     pol_last);
                 }
             }
             const bool part = full_mask != (1u << n_groups) - 1;
             if (part) {
-                // Zero-filling cp.async of the groups not wholly visible: K two
-                // dim blocks x 16 keys x 8 chunks, V 16 keys x 8 chunks.
+                // Zero-filling cp.async of the groups not wholly visible:
+                // n_db dim blocks x 16 keys x 8 chunks each.
                 for (int i = 0; i < n_groups; ++i) {
                     if ((full_mask >> i) & 1) continue;
                     const int pg = g_first + i;
@@ -364,15 +380,13 @@ __global__ void __launch_bounds__(384, 1)
                     const int blk = min(max(__shfl_sync(0xffffffffu, win_cur, wl + pg), 0), p.NB - 1);
                     const uint16_t* src0 =
                         cache + (long long)blk * p.c_s0 + (long long)(jg % p.BS) * p.c_s1 + (long long)g * p.c_s2;
-                    const int n_copy = is_v ? 128 : 256;
-                    for (int c = lane; c < n_copy; c += 32) {
-                        const int db = is_v ? rank : (c >> 7);
+                    for (int c = lane; c < n_db * 128; c += 32) {
+                        const int dbl = c >> 7;
                         const int row = (c >> 3) & 15, chunk = c & 7;
                         const bool valid = jg + row >= lo && jg + row < hi;
-                        const uint16_t* src = src0 + (long long)row * p.c_s1 + 64 * db + chunk * 8;
-                        const uint32_t dst =
-                            smem_u32(is_v ? tile + pg * 2048 : tile + db * (C::kKBytes / 2) + i * 2048) +
-                            sw128_offset((uint32_t)row, (uint32_t)chunk);
+                        const uint16_t* src = src0 + (long long)row * p.c_s1 + 64 * (db_first + dbl) + chunk * 8;
+                        const uint32_t dst = smem_u32(tile + dbl * db_stride + (is_v ? pg : i) * 2048) +
+                                             sw128_offset((uint32_t)row, (uint32_t)chunk);
                         cp_async_16(dst, valid ? src : cache, valid ? 16u : 0u, pol_last);
                     }
                 }
@@ -380,12 +394,12 @@ __global__ void __launch_bounds__(384, 1)
             }
             if (pend >= 0) retire(part ? 1 : 0);
             if (part) {
-                pend = slot;
+                pend = jj & 1;
             } else {
                 // Only TMA boxes: their bytes complete the phase, the arrival
                 // needs no cluster-scope release (which costs ~1k cycles).
                 __syncwarp();
-                if (lane == 0) mbar_arrive_remote(full_bar[slot]);
+                if (lane == 0) mbar_arrive_remote(full_bar[jj & 1]);
             }
         }
         if (pend >= 0) retire(0);
@@ -427,57 +441,58 @@ __global__ void __launch_bounds__(384, 1)
         if (rank == 0 && lane == 0 && n_it > 0) {
             constexpr uint32_t idS = umma_idesc_bf16(256, C::BN, false);
             constexpr uint32_t idPV = umma_idesc_bf16(256, C::D, true);
+            constexpr int KS = C::D / 16;  // K-steps of S
             bool ok = mbar_wait(&bars->q_full, 0, p.timeout_ns, kSitePrefillLoadQ, p.err);
-            // Descriptors: Q (K-major, 2 dim blocks), K half (K-major), V half
-            // (MN-major, one 64-dim block per CTA).  A descriptor's low bits
-            // hold address / 16, so a byte offset adds offset / 16.
+            // Descriptors: Q (K-major, kDB dim blocks), K half (K-major), V half
+            // (MN-major, kVB 64-dim blocks 16 KB apart).  A descriptor's low
+            // bits hold address / 16, so a byte offset adds offset / 16.
             const uint64_t dQ = umma_desc_sw128(smem_u32(sQ), 16, 1024);
             const uint64_t dK0 = umma_desc_sw128(smem_u32(sK), 16, 1024);
-            const uint64_t dV0 = umma_desc_sw128(smem_u32(sV), 8192, 1024);
-            uint64_t aQ[8];
+            const uint64_t dV0 = umma_desc_sw128(smem_u32(sV), 128 * 128, 1024);
+            uint64_t aQ[KS];
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                aQ[kk] = dQ + (uint64_t)(((kk >> 2) * (C::kQBytes / 2) + (kk & 3) * 32) >> 4);
-            // S_jj = Q K^T into S buffer jj % 2 (K slot jj % 2).
+            for (int kk = 0; kk < KS; ++kk)
+                aQ[kk] = dQ + (uint64_t)(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
+            // S_jj = Q K^T into S buffer jj % 2, K from ring slot jj % kRing.
             auto issue_s = [&](int jj) {
-                const int ks = jj & 1;
-                uint64_t bK[8];
+                const int sb = jj & 1, ks = jj % C::kRing;
+                uint64_t bK[KS];
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    bK[kk] = dK0 + (uint64_t)((ks * C::kKBytes + (kk >> 2) * (C::kKBytes / 2) + (kk & 3) * 32) >> 4);
-                ok = ok && mbar_wait(&bars->k_full[ks], (uint32_t)((jj >> 1) & 1), p.timeout_ns, kSitePrefillKFull,
-                                     p.err);
+                for (int kk = 0; kk < KS; ++kk)
+                    bK[kk] = dK0 + (uint64_t)((ks * C::kKBytes + (kk >> 2) * (64 * 128) + (kk & 3) * 32) >> 4);
+                ok = ok && mbar_wait(&bars->k_full[jj & 1], (uint32_t)((jj >> 1) & 1), p.timeout_ns,
+                                     kSitePrefillKFull, p.err);
                 if (!ok) return;
                 tc_fence_after();
-                const uint32_t sd = tmem + ks * C::BN;
+                const uint32_t sd = tmem + sb * C::BN;
                 umma2_ss<0>(sd, aQ[0], bK[0], idS);
 #pragma unroll
-                for (int kk = 1; kk < 8; ++kk) umma2_ss<1>(sd, aQ[kk], bK[kk], idS);
-                umma2_commit_both(&bars->s_full[ks]);
+                for (int kk = 1; kk < KS; ++kk) umma2_ss<1>(sd, aQ[kk], bK[kk], idS);
+                umma2_commit_both(&bars->s_full[sb]);
             };
             // O += P_t V_t: P from S buffer t % 2 (keys [64 h, 64 h + 64) in
             // columns [64 h, 64 h + 32)), V from V slot t % 2.  The MMAs of this
             // thread run in issue order, so S_{t+2}, issued after PV_t,
             // overwrites the buffer only once PV_t has read P_t.
             auto issue_pv = [&](int t) {
-                const int vs = t & 1;
+                const int pb = t & 1, vs = t % C::kRing;
                 uint64_t bV[8];
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) bV[kk] = dV0 + (uint64_t)((vs * C::kVBytes + kk * 2048) >> 4);
-                ok = ok && mbar_wait(&bars->p_full[vs], (uint32_t)((t >> 1) & 1), p.timeout_ns, kSitePrefillPFull,
+                ok = ok && mbar_wait(&bars->p_full[pb], (uint32_t)((t >> 1) & 1), p.timeout_ns, kSitePrefillPFull,
                                      p.err);
-                ok = ok && mbar_wait(&bars->v_full[vs], (uint32_t)((t >> 1) & 1), p.timeout_ns, kSitePrefillVFull,
+                ok = ok && mbar_wait(&bars->v_full[t & 1], (uint32_t)((t >> 1) & 1), p.timeout_ns, kSitePrefillVFull,
                                      p.err);
                 if (!ok) return;
                 tc_fence_after();
-                const uint32_t pcol = tmem + vs * C::BN, od = tmem + C::kOCol;
+                const uint32_t pcol = tmem + pb * C::BN, od = tmem + C::kOCol;
                 if (t > 0)
                     umma2_ts<1>(od, pcol, bV[0], idPV);
                 else
                     umma2_ts<0>(od, pcol, bV[0], idPV);
 #pragma unroll
                 for (int kk = 1; kk < 8; ++kk) umma2_ts<1>(od, pcol + 64 * (kk >> 2) + 8 * (kk & 3), bV[kk], idPV);
-                umma2_commit_both(&bars->o_done[vs]);
+                umma2_commit_both(&bars->o_done[pb]);
             };
             for (int jj = 0; jj < n_it && ok; ++jj) {
                 issue_s(jj);
@@ -774,33 +789,14 @@ __global__ void __launch_bounds__(384, 1)
                      : "memory");
 }
 
-}  // namespace
-
-int prefill_pair_smem_bytes() { return 1024 + PairCfg::kData + (int)sizeof(PairBars); }
-
-LaunchShape prefill_pair_shape(const AttnParams& p) {
-    LaunchShape s;
-    const int tpt = 128 / p.G;
-    const int qtiles = (p.max_seqlen_q + tpt - 1) / tpt;
-    if (p.B <= kCompactMaxB) {
-        // Pairs with rows: at most ceil(qtiles / 2) per request, and at most
-        // one partly filled pair per request beyond T / (2 * tpt) full ones.
-        const long long per_req = (qtiles + 1) / 2;
-        const long long by_rows = ((long long)p.T + 2 * tpt - 1) / (2 * tpt) + p.B;
-        const long long n_cl = per_req * p.B < by_rows ? per_req * p.B : by_rows;
-        s.grid = dim3((unsigned)(n_cl * 2), p.Hk, p.num_splits);
-    } else {
-        s.grid = dim3((unsigned)((qtiles + 1) / 2 * 2), p.Hk, p.B * p.num_splits);
-    }
-    s.block = PairCfg::kThreads;
-    s.smem = prefill_pair_smem_bytes();
-    s.nstage = 2;
-    return s;
+template <int D>
+int prefill_pair_smem_bytes() {
+    return 1024 + PairCfg<D>::kData + (int)sizeof(PairBars);
 }
 
-cudaError_t launch_prefill_pair(const AttnParams& p, const CUtensorMap* maps, const LaunchShape& s,
-                                cudaStream_t stream) {
-    auto kern = prefill_pair_kernel;
+template <int D>
+cudaError_t launch_pair_t(const AttnParams& p, const CUtensorMap* maps, const LaunchShape& s, cudaStream_t stream) {
+    auto kern = prefill_pair_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, s.smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -818,6 +814,35 @@ cudaError_t launch_prefill_pair(const AttnParams& p, const CUtensorMap* maps, co
     e = cudaLaunchKernelEx(&cfg, kern, p, maps[0], maps[1], maps[2], maps[3]);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+}  // namespace
+
+LaunchShape prefill_pair_shape(const AttnParams& p) {
+    LaunchShape s;
+    const int tpt = 128 / p.G;
+    const int qtiles = (p.max_seqlen_q + tpt - 1) / tpt;
+    if (p.B <= kCompactMaxB) {
+        // Pairs with rows: at most ceil(qtiles / 2) per request, and at most
+        // one partly filled pair per request beyond T / (2 * tpt) full ones.
+        const long long per_req = (qtiles + 1) / 2;
+        const long long by_rows = ((long long)p.T + 2 * tpt - 1) / (2 * tpt) + p.B;
+        const long long n_cl = per_req * p.B < by_rows ? per_req * p.B : by_rows;
+        s.grid = dim3((unsigned)(n_cl * 2), p.Hk, p.num_splits);
+    } else {
+        s.grid = dim3((unsigned)((qtiles + 1) / 2 * 2), p.Hk, p.B * p.num_splits);
+    }
+    s.block = 384;
+    s.smem = p.D == 256 ? prefill_pair_smem_bytes<256>() : prefill_pair_smem_bytes<128>();
+    s.nstage = p.D == 256 ? PairCfg<256>::kRing : PairCfg<128>::kRing;
+    return s;
+}
+
+cudaError_t launch_prefill_pair(const AttnParams& p, const CUtensorMap* maps, const LaunchShape& s,
+                                cudaStream_t stream) {
+    if (p.D == 128) return launch_pair_t<128>(p, maps, s, stream);
+    if (p.D == 256) return launch_pair_t<256>(p, maps, s, stream);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace relattn
