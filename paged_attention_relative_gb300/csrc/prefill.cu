@@ -13,12 +13,14 @@
 //   warps 0, 2 producers: warp 0 loads the K tiles, warp 2 the V tiles,
 //              each into its own ring so K never waits behind a V slot.  A tile
 //              arrives as 2 KB TMA boxes (16 keys x 64 dims) straight from the
-//              paged cache, one per fully visible 16-key group, multicast to
-//              the other CTA of the cluster (the two take turns issuing), with
-//              block-table entries fetched a 4-tile window ahead (one
-//              coalesced load per window); groups only partly inside the
-//              visible range go through zero-filling cp.async (proxy-fenced
-//              once landed).  Tiles are 128-byte swizzled; a slot's full
+//              paged cache, one per 16-key group that lies wholly inside the
+//              cache, multicast to the other CTA of the cluster (the two take
+//              turns issuing), with block-table entries fetched a 4-tile
+//              window ahead (one coalesced load per window).  Keys inside the
+//              cache but outside a row's window are finite and the softmax
+//              masks them, so only the one group that straddles the cache
+//              length goes through zero-filling cp.async (proxy-fenced once
+//              landed): keys past it may hold stale, non-finite data.  Tiles are 128-byte swizzled; a slot's full
 //              mbarrier takes the TMA bytes plus the producer's arrivals, its
 //              empty mbarrier one MMA commit per CTA of the cluster.  Each
 //              producer's per-tile work is on the critical path (a TMA issue
@@ -343,7 +345,7 @@ __global__ void __launch_bounds__(384, 1)
                 const int jg = key_block(jw) * C::BN + 16 * (lane & 7);
                 // (a key past the table's width, i.e. cache_seqlens > MB * BS,
                 // reads no entry: the clamp below then keeps block 0)
-                if (jg + 15 >= lo && jg < hi && jg / p.BS < p.max_blocks) v = __ldg(bt + jg / p.BS);
+                if (jg < sk && jg / p.BS < p.max_blocks) v = __ldg(bt + jg / p.BS);
             }
             return v;
         };
@@ -379,7 +381,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
             for (int pg = 0; pg < 8; ++pg) {
                 const int jg = j0 + 16 * pg;
-                if (jg >= lo && jg + 16 <= hi) full_mask |= 1u << pg;
+                if (jg + 16 <= sk) full_mask |= 1u << pg;
             }
             uint64_t* full_bar = &bars->kv_full[slot];
             uint8_t* tile = sKV + slot * C::kTileBytes;
@@ -403,7 +405,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                     for (int kk = 0; kk < kPerPage; ++kk) {
                         const int row = kk * kRows + lrow;  // key jg + row
-                        const bool valid = jg + row >= lo && jg + row < hi;
+                        const bool valid = jg + row < sk;
                         const uint32_t dst =
                             dst_tile + (16 * pg + kk * kRows) * 128 + ((cx ^ ((kk * kRows) & 7)) << 4);
                         cp_async_16(dst, valid ? src : cache, valid ? 16u : 0u, pol_last);

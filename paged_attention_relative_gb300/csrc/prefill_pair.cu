@@ -27,8 +27,10 @@
 //   warp 0     the query tile (TMA, one box per 64-dim block), then this CTA's
 //              half of every K tile into a ring (2 slots, 1 for head_dim
 //              256): 2 KB boxes (16 keys x 64 dims)
-//              straight from the paged cache, zero-filling cp.async for
-//              16-key groups only partly visible.
+//              straight from the paged cache, zero-filling cp.async only
+//              for the 16-key group that straddles the cache length (keys
+//              inside the cache but outside a row's window are finite and
+//              masked by the softmax).
 //   warp 1     bias windows: for each band tile one TMA box per 8-token
 //              sub-box into one of three (head_dim 256: two) window buffers,
 //              once the softmax has released that buffer's previous fill.
@@ -324,7 +326,7 @@ __global__ void __launch_bounds__(384, 1)
             const int jw = w0 + (lane >> 3);
             if (jw < n_it) {
                 const int jg = key_block(jw) * C::BN + 16 * (lane & 7);
-                if (jg + 15 >= lo && jg < hi && jg / p.BS < p.max_blocks) v = __ldg(bt + jg / p.BS);
+                if (jg < sk && jg / p.BS < p.max_blocks) v = __ldg(bt + jg / p.BS);
             }
             return v;
         };
@@ -350,7 +352,7 @@ __global__ void __launch_bounds__(384, 1)
             uint32_t full_mask = 0;  // bit i: group g_first + i fully visible (whole-box TMA)
             for (int i = 0; i < n_groups; ++i) {
                 const int jg = j0 + 16 * (g_first + i);
-                if (jg >= lo && jg + 16 <= hi) full_mask |= 1u << i;
+                if (jg + 16 <= sk) full_mask |= 1u << i;
             }
             uint8_t* tile = ring + slot * slot_bytes;
             const int boxes = __popc(full_mask) * n_db;
@@ -383,7 +385,7 @@ __global__ void __launch_bounds__(384, 1)
                     for (int c = lane; c < n_db * 128; c += 32) {
                         const int dbl = c >> 7;
                         const int row = (c >> 3) & 15, chunk = c & 7;
-                        const bool valid = jg + row >= lo && jg + row < hi;
+                        const bool valid = jg + row < sk;
                         const uint16_t* src = src0 + (long long)row * p.c_s1 + 64 * (db_first + dbl) + chunk * 8;
                         const uint32_t dst = smem_u32(tile + dbl * db_stride + (is_v ? pg : i) * 2048) +
                                              sw128_offset((uint32_t)row, (uint32_t)chunk);
