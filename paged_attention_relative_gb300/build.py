@@ -66,8 +66,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             list(ex.map(run, jobs))
     if force or jobs or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcuda"] if False else
-            [nvcc, *ARCH, "-shared", "-o", tmp, *objs])
+        run([nvcc, *ARCH, "-shared", "-o", tmp, *objs])
         os.replace(tmp, LIB)
     return LIB
 

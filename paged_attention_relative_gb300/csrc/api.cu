@@ -131,6 +131,47 @@ rel_attn_status make_cache_map(const rel_attn_tensor* t, CUtensorMap* map, const
     return REL_ATTN_OK;
 }
 
+// Paged cache (NB, BS, Hk, D) as a 5-D TMA view whose box is one 16-key page
+// (or half of one) of one kv head with `dbox` 64-dim blocks, 128-byte swizzle.
+// A box lands as [8-key half][64-dim block][8 keys][64 dims]: the halves, the
+// blocks and the keys of a half are separate view dimensions (keys at the slot
+// stride, blocks 128 bytes apart).  When pages are contiguous (block stride ==
+// BS * slot stride) the half index runs across blocks, (64, 8, D / 64, NB * BS
+// / 8, Hk) with a (64, 8, dbox, 2, 1) box: one box per page.  Otherwise (64,
+// BS, D / 64, Hk, NB) with a (64, 8, dbox, 1, 1) box: one box per half.
+rel_attn_status make_page_map(const rel_attn_tensor* t, int dbox, bool merged, CUtensorMap* map,
+                              const char* name) {
+    auto enc = encode_fn();
+    if (!enc) return fail(REL_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t NB = (cuuint64_t)t->shape[0], BS = (cuuint64_t)t->shape[1], Hk = (cuuint64_t)t->shape[2],
+                     D = (cuuint64_t)t->shape[3];
+    const cuuint64_t s0 = (cuuint64_t)t->stride[0] * 2, s1 = (cuuint64_t)t->stride[1] * 2,
+                     s2 = (cuuint64_t)t->stride[2] * 2;
+    cuuint64_t dims[5], strides[4];
+    cuuint32_t box[5];
+    if (merged) {
+        const cuuint64_t d[5] = {64, 8, D / 64, NB * BS / 8, Hk};
+        const cuuint64_t st[4] = {s1, 128, 8 * s1, s2};
+        const cuuint32_t bx[5] = {64, 8, (cuuint32_t)dbox, 2, 1};
+        std::memcpy(dims, d, sizeof d);
+        std::memcpy(strides, st, sizeof st);
+        std::memcpy(box, bx, sizeof bx);
+    } else {
+        const cuuint64_t d[5] = {64, BS, D / 64, Hk, NB};
+        const cuuint64_t st[4] = {s1, 128, s2, s0};
+        const cuuint32_t bx[5] = {64, 8, (cuuint32_t)dbox, 1, 1};
+        std::memcpy(dims, d, sizeof d);
+        std::memcpy(strides, st, sizeof st);
+        std::memcpy(box, bx, sizeof bx);
+    }
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, t->data, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(REL_ATTN_ERR_UNSUPPORTED, "%s: TMA descriptor rejected (CUresult %d)", name, (int)r);
+    return REL_ATTN_OK;
+}
+
 // q (T, H, D) as a 3-D TMA tensor, innermost first: (D, H, T), box (64 dims,
 // G heads, 128 / G tokens) = one 64-dim block of a GQA-packed query tile,
 // 128-byte swizzle.
@@ -544,8 +585,16 @@ rel_attn_status paged_varlen(
     const bool pair =
         prefill && (D == 256 || (D == 128 && (rel_extent == 0 || p.vec_bias) && prefill_pair_requested()));
     if (prefill) {
-        if ((st = make_cache_map(key_cache, &maps[0], "key_cache"))) return st;
-        if ((st = make_cache_map(value_cache, &maps[1], "value_cache"))) return st;
+        if (pair) {
+            if ((st = make_cache_map(key_cache, &maps[0], "key_cache"))) return st;
+            if ((st = make_cache_map(value_cache, &maps[1], "value_cache"))) return st;
+        } else {
+            // (K and V share strides, checked above.)
+            p.kv_merged = p.c_s0 == (int64_t)BS * p.c_s1 ? 1 : 0;
+            const int dbox = (int)(D / 64);
+            if ((st = make_page_map(key_cache, dbox, p.kv_merged != 0, &maps[0], "key_cache"))) return st;
+            if ((st = make_page_map(value_cache, dbox, p.kv_merged != 0, &maps[1], "value_cache"))) return st;
+        }
         // Tokens per rel_logits box: the largest divisor of the tile's 128 / G
         // tokens that is at most 8 (a box then never crosses the tile).
         const int tpt = (int)(128 / G);

@@ -102,6 +102,21 @@ __device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t n) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(n) : "memory");
 }
 
+// Non-blocking check: has the phase with this parity completed?  Cheaper than
+// try_wait when it has (a thread that issues tcgen05.mma keeps the tensor pipe
+// fed only between its waits, so every cycle there counts).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -119,7 +134,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // and the function returns false; the caller must then stop using the pipeline.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns, int site,
                                           int* err) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;
     // SM clock cycles (cheap to read); 4 cycles per ns bounds every clock up to 4 GHz.
     const long long budget = (long long)timeout_ns * 4;
     const long long t0 = clock64();
@@ -181,6 +196,20 @@ __device__ __forceinline__ void tma_load_4d_mc(void* dst, const void* desc, uint
         ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7, %8;" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(desc)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "h"(mask),
         "l"(policy)
+        : "memory");
+}
+
+// 5-D tiled load, multicast to the CTAs of ctaMask.  The paged caches are
+// read through 5-D views whose box is one 16-key page (or half of one) of
+// one kv head, all of its 64-dim blocks: far fewer TMA operations per tile
+// than one box per 64-dim block.
+__device__ __forceinline__ void tma_load_5d_mc(void* dst, const void* desc, uint64_t* bar, int c0, int c1, int c2,
+                                               int c3, int c4, uint16_t mask, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8, %9;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(desc)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+        "h"(mask), "l"(policy)
         : "memory");
 }
 
@@ -247,6 +276,16 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 // the peer's), releasing this thread's prior writes at cluster scope.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Arrive on an mbarrier given by its shared::cluster address (this CTA's or
+// another CTA's of the cluster) with the default semantics (release at CTA
+// scope); much cheaper than a release.cluster arrive.  Used only where what
+// the arrival reports has already completed in hardware: TMEM stores waited
+// with tcgen05.wait::st and fenced by tcgen05.fence::before_thread_sync, or
+// MMA reads of a buffer observed complete through a tcgen05.commit.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 // Add `bytes` to the expected transaction count of the current phase of an

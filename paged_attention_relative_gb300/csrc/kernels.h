@@ -44,6 +44,8 @@ struct AttnParams {
     int32_t nstage;
     int32_t nprod;             // decode: producer warps
     int32_t vec_bias;          // rel_logits rows 16-byte aligned (R % 8 == 0): staged by 16-byte copies
+    int32_t kv_merged;         // prefill: the caches' pages are contiguous (c_s0 == BS * c_s1), so one
+                               // 5-D TMA box holds a whole 16-key page
     uint64_t timeout_ns;
     int* err;                  // device error word (bounded-wait timeouts)
 };
@@ -62,8 +64,10 @@ LaunchShape decode_shape(const AttnParams& p, int num_sms);
 cudaError_t launch_decode(const AttnParams& p, const LaunchShape& shape, cudaStream_t stream);
 
 // tcgen05 prefill kernel for 128-row GQA-packed query tiles.  maps[0] / maps[1]
-// describe key_cache / value_cache as 4-D TMA tensors (D, Hk, BS, NB) with a
-// (64, 1, 16, 1) box and 128-byte swizzle; maps[2] describes rel_logits as a
+// describe key_cache / value_cache as 5-D TMA views with 128-byte swizzle
+// (make_page_map): (64, 8, D / 64, NB * BS / 8, Hk) with a (64, 8, D / 64, 2, 1)
+// box when kv_merged, else (64, BS, D / 64, Hk, NB) with a (64, 8, D / 64, 1, 1)
+// box; maps[2] describes rel_logits as a
 // 3-D tensor (R, H, T) with a (prefill_bias_window(), G, bias_ts) box (only
 // read when vec_bias).
 LaunchShape prefill_shape(const AttnParams& p);

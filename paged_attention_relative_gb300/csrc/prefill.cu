@@ -12,20 +12,24 @@
 // Warp roles (384 threads):
 //   warps 0, 2 producers: warp 0 loads the K tiles, warp 2 the V tiles,
 //              each into its own ring so K never waits behind a V slot.  A tile
-//              arrives as 2 KB TMA boxes (16 keys x 64 dims) straight from the
-//              paged cache, one per 16-key group that lies wholly inside the
+//              arrives straight from the paged cache as TMA boxes of one
+//              16-key page each (all 64-dim blocks of one kv head, through a
+//              5-D view of the cache; two boxes of 8 keys when the cache's
+//              pages are not contiguous), one per page wholly inside the
 //              cache, multicast to the other CTA of the cluster (the two take
 //              turns issuing), with block-table entries fetched a 4-tile
-//              window ahead (one coalesced load per window).  Keys inside the
+//              window ahead (one coalesced load per window).  The TMA unit's
+//              cost is mostly per box (on GB300 about 50 cycles per box plus
+//              1.5 per 128-byte row), so whole pages rather than 64-dim blocks
+//              per box take it off the critical path.  Keys inside the
 //              cache but outside a row's window are finite and the softmax
 //              masks them, so only the one group that straddles the cache
 //              length goes through zero-filling cp.async (proxy-fenced once
-//              landed): keys past it may hold stale, non-finite data.  Tiles are 128-byte swizzled; a slot's full
-//              mbarrier takes the TMA bytes plus the producer's arrivals, its
-//              empty mbarrier one MMA commit per CTA of the cluster.  Each
-//              producer's per-tile work is on the critical path (a TMA issue
-//              costs ~90 cycles per box even spread over lanes), so the loop
-//              keeps nothing else in it: no global loads, no divisions.
+//              landed): keys past it may hold stale, non-finite data.  Tiles
+//              are 128-byte swizzled; a slot's full mbarrier takes the TMA
+//              bytes plus the producer's arrivals, its empty mbarrier one MMA
+//              commit per CTA of the cluster.  The producer loop keeps
+//              nothing else in it: no global loads, no divisions.
 //   warp 1     bias windows: for each band tile (one that reaches some row's
 //              bias band) it stages that tile's rel_logits by TMA into one of
 //              two window buffers (one with D = 64) once the softmax warps
@@ -89,8 +93,15 @@ template <int D>
 struct PrefillCfg {
     static constexpr int BN = 128;                  // keys per tile (query tiles are 128 rows)
     static constexpr int kDB = D / 64;              // 64-dim (128-byte) column blocks
-    static constexpr int kBlk = 128 * 128;          // one 128-row x 128-byte block
-    static constexpr int kTileBytes = kDB * kBlk;   // a K or V tile
+    // A K or V tile in shared memory: 8 pages of 16 keys, each two halves of
+    // 8 keys, each half kDB swizzle atoms (8 keys x 64 dims, 1 KB): key
+    // 16 p + 8 h + r, dims [64 c, 64 c + 64) at p * kPage + h * kHalf + c * 1024
+    // + r * 128.  This is the order a 5-D TMA box of one page lands in, and
+    // a canonical 128-byte-swizzled operand: K-major (keys = N) with 8-key
+    // groups kHalf apart, or MN-major (dims = N) with 64-dim blocks 1 KB apart.
+    static constexpr int kHalf = kDB * 1024;
+    static constexpr int kPage = 2 * kHalf;
+    static constexpr int kTileBytes = 8 * kPage;
     static constexpr int kMmaWarp = 3;
     static constexpr int kSoftThreads = 256;        // warps 4-11
     static constexpr int kThreads = 384;
@@ -115,9 +126,9 @@ struct PrefillCfg {
 struct PrefillBars {
     uint64_t q_full;
     uint64_t kv_full[10];
-    uint64_t kv_empty[10];
+    uint64_t kv_empty[10];   // this CTA's MMAs have read the slot's current use (a local commit)
+    uint64_t kv_peer[10];    // the other CTA's MMAs have (its producer forwards its kv_empty)
     uint64_t s_full[2];
-    uint64_t p_full[2];
     uint64_t x_full[2];      // per tile parity: every softmax warp has published its half-row maxima
     uint64_t o_done;   // one phase per PV tile (rescale waits, never more than one phase behind)
     uint64_t o_final;  // single phase: every MMA of the CTA has completed
@@ -260,12 +271,15 @@ __global__ void __launch_bounds__(384, 1)
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, C::kSoftThreads / 2);
         for (int i = 0; i < C::kStages; ++i) {
-            mbar_init(&bars->kv_full[i], 33);  // producer lanes + the expect_tx arrival
-            mbar_init(&bars->kv_empty[i], n_act);  // one MMA commit per active CTA of the cluster
+            // producer lanes + the expect_tx arrival; a V slot also takes one
+            // arrival per softmax warp once P of its tile is in TMEM, so the
+            // MMA thread waits once before each PV
+            mbar_init(&bars->kv_full[i], i < C::kKRing ? 33 : 33 + C::kSoftThreads / 32);
+            mbar_init(&bars->kv_empty[i], 1);
+            mbar_init(&bars->kv_peer[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->s_full[i], 1);
-            mbar_init(&bars->p_full[i], C::kSoftThreads);
             mbar_init(&bars->x_full[i], C::kSoftThreads / 32);
         }
         mbar_init(&bars->o_done, 1);
@@ -298,15 +312,14 @@ __global__ void __launch_bounds__(384, 1)
 
     if (warp == 0 || warp == 2) {
         // ------------------------------------------------------ Q/K and V producers
-        // Warp 0 loads Q, then the K ring; warp 2 the V ring, so a K tile
-        // never queues behind a V slot the softmax still holds.
-        // Q: 16-byte cp.async per (row, chunk), GQA-packed rows, zero-fill
-        // past the tile's rows.  K/V: one TMA box (16 keys x 64 dims, 2 KB)
-        // per fully visible 16-key group and 64-dim block, multicast to the
-        // cluster (the active CTAs take turns issuing them); groups that are
-        // only partly visible (or not at all) go through zero-filling
-        // cp.async, so V rows the softmax gives weight 0 hold zeros, never
-        // stale cache contents (0 * NaN would poison the row).
+        // Warp 0 loads the K ring, warp 2 the V ring, so a K tile never
+        // queues behind a V slot the softmax still holds.  One TMA box per
+        // 16-key page wholly inside the cache (both 8-key halves in one box
+        // when the cache's pages are contiguous, else one box per half),
+        // multicast to the cluster, the active CTAs taking turns; the group
+        // that straddles the cache length goes through zero-filling
+        // cp.async, so V rows past it hold zeros, never stale cache contents
+        // (0 * NaN would poison the row).
         const bool is_v = warp == 2;
         constexpr int kChunks = D / 8;
         constexpr int kRows = 32 / kChunks;
@@ -316,7 +329,7 @@ __global__ void __launch_bounds__(384, 1)
         const CUtensorMap* tmap = is_v ? &tm_v : &tm_k;
         const int32_t* bt = p.block_table + (size_t)b * p.bt_stride;
         const uint64_t pol_last = l2_policy_evict_last();
-        const uint32_t col_off = (lchunk >> 3) * C::kBlk;
+        const uint32_t col_off = (lchunk >> 3) * 1024;
         // Within a 16-row group, row (kk*kRows + lrow) & 7 == ((kk*kRows) & 7) | lrow,
         // so the 128-byte swizzle is the per-lane constant cx XOR a compile-time one.
         const long long lane_off = (long long)lrow * p.c_s1 + lchunk * 8;
@@ -350,21 +363,36 @@ __global__ void __launch_bounds__(384, 1)
             return v;
         };
         int win_cur = load_win(0), win_nxt = load_win(4);
-        // TMA lanes: lane -> (16-key group lane / kDB, 64-dim block lane % kDB).
-        const int t_pg = lane / C::kDB, t_db = lane % C::kDB;
+        // TMA lanes: lane -> (16-key group lane / nbox, half lane % nbox),
+        // nbox = 1 when a box holds the whole page.
+        const int nbox = p.kv_merged ? 1 : 2;
+        const int t_pg = lane / nbox, t_h = lane % nbox;
         const int ring0 = is_v ? C::kKRing : 0;
         const int ring = is_v ? C::kVRing : C::kKRing;
         int sidx = 0;
         uint32_t eph = 1;  // parity of the empty phase to wait for
+        // The slot's previous use is released by this CTA's MMA commit
+        // (kv_empty) and, with two active CTAs, by the other CTA's, which its
+        // producer forwards here (kv_peer); this producer forwards its own in
+        // turn.  (The MMA thread then only commits locally: a multicast
+        // commit stalls the tensor pipe.)
+        const uint32_t peer_bar0 = mapa_shared(smem_u32(&bars->kv_peer[ring0]), (uint32_t)crank ^ 1u);
+        // Never block on a full ring while holding copies whose landing has
+        // not been signalled: the consumer may be waiting for exactly those.
+        auto wait_slot = [&](uint64_t* bar, uint32_t par, int site) {
+            if (!mbar_try_wait(bar, par)) {
+                if (pend) retire(0);
+                if (!mbar_wait(bar, par, p.timeout_ns, site, p.err)) bars->abort = 1;
+            }
+        };
+        auto release_to_peer = [&](int slot, uint32_t par) {
+            if (lane == 0) mbar_arrive_remote(peer_bar0 + (uint32_t)(slot - ring0) * 8u);
+            wait_slot(&bars->kv_peer[slot], par, kSitePrefillKEmpty);
+        };
         for (int jj = 0; jj < n_it; ++jj) {
             const int slot = ring0 + sidx;
-            // Never block on a full ring while holding copies whose landing has
-            // not been signalled: the consumer may be waiting for exactly those.
-            if (!mbar_try_wait(&bars->kv_empty[slot], eph)) {
-                if (pend) retire(0);
-                if (!mbar_wait(&bars->kv_empty[slot], eph, p.timeout_ns, kSitePrefillKEmpty, p.err))
-                    bars->abort = 1;
-            }
+            wait_slot(&bars->kv_empty[slot], eph, kSitePrefillKEmpty);
+            if (jj >= ring && n_act == 2) release_to_peer(slot, eph);
             if (++sidx == ring) {
                 sidx = 0;
                 eph ^= 1;
@@ -388,10 +416,16 @@ __global__ void __launch_bounds__(384, 1)
             if (lane == 0) mbar_arrive_expect_tx(full_bar, (uint32_t)__popc(full_mask) * C::kDB * 2048u);
             __syncwarp();
             const int blk_t = min(max(__shfl_sync(0xffffffffu, win_cur, wl + (t_pg & 7)), 0), p.NB - 1);
-            if (lane < 8 * C::kDB && ((full_mask >> t_pg) & 1) && lane % n_act == my_idx) {
-                const int jg = j0 + 16 * t_pg;
-                tma_load_4d_mc(tile + t_db * C::kBlk + t_pg * 16 * 128, tmap, full_bar, 64 * t_db, g, jg % p.BS,
-                               blk_t, mc_mask, pol_last);
+            if (lane < 8 * nbox && ((full_mask >> t_pg) & 1) && lane % n_act == my_idx) {
+                const int slot_in_blk = (j0 + 16 * t_pg) % p.BS;
+                // merged view (64, 8, kDB, NB * BS / 8, Hk): half-page blk * BS / 8 + slot / 8;
+                // split view (64, BS, kDB, Hk, NB): slot, head, block.
+                if (p.kv_merged)
+                    tma_load_5d_mc(tile + t_pg * C::kPage, tmap, full_bar, 0, 0, 0,
+                                   blk_t * (p.BS >> 3) + (slot_in_blk >> 3), g, mc_mask, pol_last);
+                else
+                    tma_load_5d_mc(tile + t_pg * C::kPage + t_h * C::kHalf, tmap, full_bar, 0, slot_in_blk + 8 * t_h,
+                                   0, g, blk_t, mc_mask, pol_last);
             }
             const bool part = full_mask != 0xffu;
             if (part) {
@@ -406,8 +440,8 @@ __global__ void __launch_bounds__(384, 1)
                     for (int kk = 0; kk < kPerPage; ++kk) {
                         const int row = kk * kRows + lrow;  // key jg + row
                         const bool valid = jg + row < sk;
-                        const uint32_t dst =
-                            dst_tile + (16 * pg + kk * kRows) * 128 + ((cx ^ ((kk * kRows) & 7)) << 4);
+                        const uint32_t dst = dst_tile + pg * C::kPage + ((kk * kRows) >> 3) * C::kHalf +
+                                             ((kk * kRows) & 7) * 128 + ((cx ^ ((kk * kRows) & 7)) << 4);
                         cp_async_16(dst, valid ? src : cache, valid ? 16u : 0u, pol_last);
                         src += row_step;
                     }
@@ -423,14 +457,15 @@ __global__ void __launch_bounds__(384, 1)
             }
         }
         if (pend) retire(0);
-        // Wait until every active CTA has released each slot for the last
-        // time: afterwards no peer commit is still travelling to this CTA.
+        // Wait until both CTAs have released each slot for the last time
+        // (forwarding this CTA's release): afterwards no arrival from the
+        // other CTA is still travelling to this one.
         if (!__any_sync(0xffffffffu, aborted(bars))) {
             for (int i = 0; i < min(ring, n_it); ++i) {
                 const int last = i + ring * ((n_it - 1 - i) / ring);
-                if (!mbar_wait(&bars->kv_empty[ring0 + i], (last / ring) & 1, p.timeout_ns,
-                               kSitePrefillKEmpty, p.err))
-                    bars->abort = 1;
+                const uint32_t par = (uint32_t)(last / ring) & 1u;
+                wait_slot(&bars->kv_empty[ring0 + i], par, kSitePrefillKEmpty);
+                if (n_act == 2) release_to_peer(ring0 + i, par);
             }
         }
     } else if (warp == 1) {
@@ -478,8 +513,8 @@ __global__ void __launch_bounds__(384, 1)
             // issue back to back (any instruction between two of them delays
             // the tensor pipe).  A descriptor's low bits hold address / 16, so
             // a byte offset inside shared memory adds offset / 16.
-            const uint64_t dK0 = umma_desc_sw128(aKV, 16, 1024);
-            const uint64_t dV0 = umma_desc_sw128(aKV, C::kBlk, 1024);
+            const uint64_t dK0 = umma_desc_sw128(aKV, 16, C::kHalf);
+            const uint64_t dV0 = umma_desc_sw128(aKV, 1024, C::kHalf);
             const uint32_t aq = tmem + C::kQCol;
             // P_t sits in S buffer t % 2: keys [64h, 64h + 64) in columns
             // [64h, 64h + 32) of the buffer.  The MMAs of this thread run in
@@ -491,11 +526,11 @@ __global__ void __launch_bounds__(384, 1)
                 const uint64_t dv = dV0 + (uint64_t)((slot * C::kTileBytes) >> 4);
                 uint64_t dV[C::BN / 16];
 #pragma unroll
-                for (int kk = 0; kk < C::BN / 16; ++kk) dV[kk] = dv + (uint64_t)((kk * 16 * 128) >> 4);
+                for (int kk = 0; kk < C::BN / 16; ++kk) dV[kk] = dv + (uint64_t)((kk * C::kPage) >> 4);
                 const uint32_t pcol = tmem + pb * C::BN;
                 const uint32_t od = tmem + C::kOCol;
-                ok = ok && mbar_wait(&bars->p_full[pb], (t >> 1) & 1, p.timeout_ns, kSitePrefillPFull, p.err);
-                ok = ok && mbar_wait(&bars->kv_full[slot], (t / C::kVRing) & 1, p.timeout_ns, kSitePrefillVFull,
+                // V_t has landed and every softmax warp has written its part of P_t.
+                ok = ok && mbar_wait(&bars->kv_full[slot], (t / C::kVRing) & 1, p.timeout_ns, kSitePrefillPFull,
                                      p.err);
                 if (!ok) return;
                 tc_fence_after();
@@ -507,7 +542,7 @@ __global__ void __launch_bounds__(384, 1)
                 for (int kk = 1; kk < C::BN / 16; ++kk)
                     umma_ts<1>(od, pcol + 64 * (kk >> 2) + 8 * (kk & 3), dV[kk], idPV);
                 umma_commit(&bars->o_done);
-                umma_commit_mc(&bars->kv_empty[slot], mc_mask);
+                umma_commit(&bars->kv_empty[slot]);
             };
             // Tile jj's S buffer, K slot and V slot depend on jj % 2 only when
             // both rings have two slots: unroll by two so every descriptor and
@@ -519,7 +554,7 @@ __global__ void __launch_bounds__(384, 1)
                 const uint64_t dk = dK0 + (uint64_t)((slot_rt * C::kTileBytes) >> 4);
                 uint64_t dK[D / 16];
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) dK[kk] = dk + (uint64_t)((((kk >> 2) * C::kBlk) + (kk & 3) * 32) >> 4);
+                for (int kk = 0; kk < D / 16; ++kk) dK[kk] = dk + (uint64_t)((((kk >> 2) * 1024) + (kk & 3) * 32) >> 4);
                 const uint32_t sd = tmem + P * C::BN;
                 (void)slot;
                 ok = ok && mbar_wait(&bars->kv_full[slot_rt], (jj / C::kKRing) & 1, p.timeout_ns, kSitePrefillKFull,
@@ -530,7 +565,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                 for (int kk = 1; kk < D / 16; ++kk) umma_ts<1>(sd, aq + 8 * kk, dK[kk], idS);
                 umma_commit(&bars->s_full[P]);
-                umma_commit_mc(&bars->kv_empty[slot_rt], mc_mask);
+                umma_commit(&bars->kv_empty[slot_rt]);
             };
             using I0 = std::integral_constant<int, 0>;
             using I1 = std::integral_constant<int, 1>;
@@ -788,7 +823,8 @@ __global__ void __launch_bounds__(384, 1)
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&bars->p_full[sb]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->kv_full[C::kKRing + jj % C::kVRing]);
         }
 
         // Epilogue: O / l, with l the sum of the two halves' partial sums.

@@ -110,14 +110,6 @@ __device__ __forceinline__ bool aborted(const PairBars* bars) {
     return *reinterpret_cast<const volatile int*>(&bars->abort) != 0;
 }
 
-// Arrive on an mbarrier given by its shared::cluster address (this CTA's or
-// the peer's) with the default release semantics at CTA scope.  The
-// softmax's hand-off of P: the TMEM stores are complete (tcgen05.wait::st)
-// and ordered before it by tcgen05.fence::before_thread_sync.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
 constexpr int kCompactMaxB = 256;
 
 // Cluster ci of a compact launch -> (request, top query tile of its pair), or
