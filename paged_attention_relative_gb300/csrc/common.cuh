@@ -199,6 +199,17 @@ __device__ __forceinline__ void tma_load_4d_mc(void* dst, const void* desc, uint
         : "memory");
 }
 
+// 5-D tiled load into this CTA's shared memory.
+__device__ __forceinline__ void tma_load_5d(void* dst, const void* desc, uint64_t* bar, int c0, int c1, int c2, int c3,
+                                            int c4, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(desc)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+        "l"(policy)
+        : "memory");
+}
+
 // 5-D tiled load, multicast to the CTAs of ctaMask.  The paged caches are
 // read through 5-D views whose box is one 16-key page (or half of one) of
 // one kv head, all of its 64-dim blocks: far fewer TMA operations per tile
@@ -233,6 +244,15 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 // Every thread of every CTA in the cluster (warp-converged).
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The two halves of cluster_sync, for work that may go on between them
+// (each thread arrives, then waits, before it arrives again).
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tma_load_3d(void* dst, const void* desc, uint64_t* bar, int c0, int c1, int c2) {

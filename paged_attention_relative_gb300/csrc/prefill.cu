@@ -142,25 +142,34 @@ __device__ __forceinline__ bool aborted(const PrefillBars* bars) {
     return *reinterpret_cast<const volatile int*>(&bars->abort) != 0;
 }
 
-__device__ __forceinline__ int floor_div8(int x) { return x >= 0 ? x >> 3 : -((-x + 7) >> 3); }
-
 // Batches up to this size launch one cluster per (request, pair of query
 // tiles) that has rows, found by a scan over cu_seqlens_q; larger ones launch
 // max_seqlen_q's tile count for every request and let empty clusters leave.
 constexpr int kCompactMaxB = 256;
 
-// Cluster ci of a compact launch -> (request, top query tile of its pair), or
-// request -1 past the last pair.  Requests in order; within a request the
-// pairs go from the last (most keys) to the first.  Warp-collective: every
-// lane gets the same answer.
-__device__ __forceinline__ int2 compact_cluster_tile(const int32_t* cu, int B, int TPT, int ci) {
+// A cluster's work: request b, the top query tile of its pair, the request's
+// first query token q0, its query and cache lengths.
+struct ClusterWork {
+    int b, top, q0, sq, sk;
+};
+
+// Cluster ci of a compact launch -> its work, or request -1 past the last
+// pair.  Requests in order; within a request the pairs go from the last (most
+// keys) to the first.  The lengths come from the same scan (one round of
+// independent loads: they are on the CTA's start-up path).  Warp-collective:
+// every lane gets the same answer.
+__device__ __forceinline__ ClusterWork compact_cluster_work(const int32_t* cu, const int32_t* seqk, int B, int TPT,
+                                                            int ci) {
     const int lane = threadIdx.x & 31;
     int base = 0;
     for (int b0 = 0; b0 < B; b0 += 32) {
         const int bb = b0 + lane;
-        int n = 0;
+        int n = 0, c0 = 0, c1 = 0, kl = 0;
         if (bb < B) {
-            const int nt = (__ldg(cu + bb + 1) - __ldg(cu + bb) + TPT - 1) / TPT;
+            c0 = __ldg(cu + bb);
+            c1 = __ldg(cu + bb + 1);
+            kl = __ldg(seqk + bb);
+            const int nt = (c1 - c0 + TPT - 1) / TPT;
             n = (nt + kCluster - 1) / kCluster;
         }
         int inc = n;
@@ -175,17 +184,26 @@ __device__ __forceinline__ int2 compact_cluster_tile(const int32_t* cu, int B, i
             const int first = base + __shfl_sync(0xffffffffu, inc - n, src);
             const int nb = __shfl_sync(0xffffffffu, n, src);
             const int k = nb - 1 - (ci - first);
-            return make_int2(b0 + src, k * kCluster + kCluster - 1);
+            ClusterWork w;
+            w.b = b0 + src;
+            w.top = k * kCluster + kCluster - 1;
+            w.q0 = __shfl_sync(0xffffffffu, c0, src);
+            w.sq = __shfl_sync(0xffffffffu, c1 - c0, src);
+            w.sk = __shfl_sync(0xffffffffu, kl, src);
+            return w;
         }
         base += tot;
     }
-    return make_int2(-1, 0);
+    ClusterWork none;
+    none.b = -1;
+    none.top = none.q0 = none.sq = none.sk = 0;
+    return none;
 }
 
 // VEC: rel_logits rows are 16-byte aligned (R % 8 == 0), so bias windows are
 // staged by 16-byte copies; otherwise the bias is read per element.
 template <int D, bool VEC>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     prefill_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_rel) {
     using C = PrefillCfg<D>;
@@ -201,21 +219,25 @@ __global__ void __launch_bounds__(384, 1)
     const int crank = (int)cluster_ctarank();
     const int g = blockIdx.y;
     const int S = p.num_splits;
-    int qt, b, split;
+    int qt, b, split, q0, sq, sk;
     if (p.B <= kCompactMaxB) {
-        const int2 ct = compact_cluster_tile(p.cu_seqlens_q, p.B, TPT, (int)(blockIdx.x / kCluster));
-        if (ct.x < 0) return;  // past the last pair (the same in every CTA of the cluster)
-        b = ct.x;
-        qt = ct.y - crank;
+        const ClusterWork w =
+            compact_cluster_work(p.cu_seqlens_q, p.cache_seqlens, p.B, TPT, (int)(blockIdx.x / kCluster));
+        if (w.b < 0) return;  // past the last pair (the same in every CTA of the cluster)
+        b = w.b;
+        qt = w.top - crank;
         split = blockIdx.z;
+        q0 = w.q0;
+        sq = w.sq;
+        sk = w.sk;
     } else {
         qt = gridDim.x - 1 - blockIdx.x;  // longest tiles first
         b = blockIdx.z / S;
         split = blockIdx.z % S;
+        q0 = p.cu_seqlens_q[b];
+        sq = p.cu_seqlens_q[b + 1] - q0;
+        sk = p.cache_seqlens[b];
     }
-    const int q0 = p.cu_seqlens_q[b];
-    const int sq = p.cu_seqlens_q[b + 1] - q0;
-    const int sk = p.cache_seqlens[b];
     const int i0 = qt * TPT;
     const int i1 = min(sq, i0 + TPT);
     const int n_rows = max(i1 - i0, 0) * G;
@@ -261,12 +283,51 @@ __global__ void __launch_bounds__(384, 1)
     const int n_it = t_end - t_begin;
     auto key_block = [&](int jj) { return kb_first + t_end - 1 - jj; };  // last tile first
     // Does key tile [j0, j0+128) reach the bias band 0 <= pos - j < R of some row?
-    constexpr bool vec_bias = VEC;
     auto band_tile = [&](int j0) { return R > 0 && pos_max - j0 >= 0 && pos_min - (j0 + C::BN - 1) < R; };
 
     // A cluster with no rows at all touches no shared memory of another CTA:
     // both of its CTAs leave at once (the same test in both).
     if (active == 0) return;
+
+    // Start-up latencies overlap the barrier and cluster set-up: warps 4-7
+    // load their query rows into registers (they go to TMEM once it is
+    // allocated), the producers their first block-table windows.
+    uint32_t qv[D / 64][32];
+    if (me_active && warp >= 4 && warp < 8) {
+        const int r = (warp & 3) * 32 + lane;
+        const bool valid = r < n_rows;
+        const int t = q0 + i0 + (valid ? r / G : 0), h = g * G + (valid ? r % G : 0);
+        const uint4* src =
+            reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.q) + (size_t)t * p.q_st + (size_t)h * p.q_sh);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+            const uint4 v = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+            qv[c / 8][4 * (c % 8)] = v.x;
+            qv[c / 8][4 * (c % 8) + 1] = v.y;
+            qv[c / 8][4 * (c % 8) + 2] = v.z;
+            qv[c / 8][4 * (c % 8) + 3] = v.w;
+        }
+    }
+    // Block-table windows of 4 tiles: lane l holds the physical block of
+    // 16-key group l % 8 of tile w0 + l / 8; the next window is fetched one
+    // window ahead (32 consecutive entries when BS is 16).
+    const int32_t* bt = p.block_table + (size_t)b * p.bt_stride;
+    auto load_win = [&](int w0) -> int {
+        int v = 0;
+        const int jw = w0 + (lane >> 3);
+        if (jw < n_it) {
+            const int jg = key_block(jw) * C::BN + 16 * (lane & 7);
+            // (a key past the table's width, i.e. cache_seqlens > MB * BS,
+            // reads no entry: the clamp below then keeps block 0)
+            if (jg < sk && jg / p.BS < p.max_blocks) v = __ldg(bt + jg / p.BS);
+        }
+        return v;
+    };
+    int win_cur = 0, win_nxt = 0;
+    if (me_active && (warp == 0 || warp == 2)) {
+        win_cur = load_win(0);
+        win_nxt = load_win(4);
+    }
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, C::kSoftThreads / 2);
@@ -291,14 +352,7 @@ __global__ void __launch_bounds__(384, 1)
         bars->abort = 0;
         fence_mbar_init();
     }
-    // Peers multicast into this CTA's ring and arrive on its barriers only
-    // after every CTA of the cluster has initialised them.
-    cluster_sync();
-    if (!me_active) {
-        cluster_sync();
-        return;
-    }
-    if (warp == C::kMmaWarp) {
+    if (me_active && warp == C::kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(&bars->tmem_base)),
                      "n"(C::kTmemCols)
@@ -308,6 +362,16 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // This CTA's barriers are initialised.  The other CTA multicasts into its
+    // ring and arrives on its barriers only after its cluster_wait has seen
+    // this arrival; until then each CTA works on its own (first fills of
+    // every ring slot are loaded by each CTA for itself).
+    cluster_arrive();
+    if (!me_active) {
+        cluster_wait();
+        cluster_sync();
+        return;
+    }
     const uint32_t tmem = bars->tmem_base;
 
     if (warp == 0 || warp == 2) {
@@ -327,7 +391,6 @@ __global__ void __launch_bounds__(384, 1)
         const int lrow = lane / kChunks, lchunk = lane % kChunks;
         const uint16_t* cache = reinterpret_cast<const uint16_t*>(is_v ? p.v_cache : p.k_cache);
         const CUtensorMap* tmap = is_v ? &tm_v : &tm_k;
-        const int32_t* bt = p.block_table + (size_t)b * p.bt_stride;
         const uint64_t pol_last = l2_policy_evict_last();
         const uint32_t col_off = (lchunk >> 3) * 1024;
         // Within a 16-row group, row (kk*kRows + lrow) & 7 == ((kk*kRows) & 7) | lrow,
@@ -348,21 +411,6 @@ __global__ void __launch_bounds__(384, 1)
             mbar_arrive(pend);
             pend = nullptr;
         };
-        // Block-table windows of 4 tiles: lane l holds the physical block of
-        // 16-key group l % 8 of tile w0 + l / 8; the next window is fetched
-        // one window ahead (32 consecutive entries when BS is 16).
-        auto load_win = [&](int w0) -> int {
-            int v = 0;
-            const int jw = w0 + (lane >> 3);
-            if (jw < n_it) {
-                const int jg = key_block(jw) * C::BN + 16 * (lane & 7);
-                // (a key past the table's width, i.e. cache_seqlens > MB * BS,
-                // reads no entry: the clamp below then keeps block 0)
-                if (jg < sk && jg / p.BS < p.max_blocks) v = __ldg(bt + jg / p.BS);
-            }
-            return v;
-        };
-        int win_cur = load_win(0), win_nxt = load_win(4);
         // TMA lanes: lane -> (16-key group lane / nbox, half lane % nbox),
         // nbox = 1 when a box holds the whole page.
         const int nbox = p.kv_merged ? 1 : 2;
@@ -390,6 +438,10 @@ __global__ void __launch_bounds__(384, 1)
             wait_slot(&bars->kv_peer[slot], par, kSitePrefillKEmpty);
         };
         for (int jj = 0; jj < n_it; ++jj) {
+            // Multicast loads and releases to the other CTA from the second
+            // use of a slot on.
+            if (jj == ring) cluster_wait();
+            const bool mc = jj >= ring;
             const int slot = ring0 + sidx;
             wait_slot(&bars->kv_empty[slot], eph, kSitePrefillKEmpty);
             if (jj >= ring && n_act == 2) release_to_peer(slot, eph);
@@ -416,16 +468,18 @@ __global__ void __launch_bounds__(384, 1)
             if (lane == 0) mbar_arrive_expect_tx(full_bar, (uint32_t)__popc(full_mask) * C::kDB * 2048u);
             __syncwarp();
             const int blk_t = min(max(__shfl_sync(0xffffffffu, win_cur, wl + (t_pg & 7)), 0), p.NB - 1);
-            if (lane < 8 * nbox && ((full_mask >> t_pg) & 1) && lane % n_act == my_idx) {
+            if (lane < 8 * nbox && ((full_mask >> t_pg) & 1) && (!mc || lane % n_act == my_idx)) {
                 const int slot_in_blk = (j0 + 16 * t_pg) % p.BS;
                 // merged view (64, 8, kDB, NB * BS / 8, Hk): half-page blk * BS / 8 + slot / 8;
                 // split view (64, BS, kDB, Hk, NB): slot, head, block.
-                if (p.kv_merged)
-                    tma_load_5d_mc(tile + t_pg * C::kPage, tmap, full_bar, 0, 0, 0,
-                                   blk_t * (p.BS >> 3) + (slot_in_blk >> 3), g, mc_mask, pol_last);
+                uint8_t* dst = tile + t_pg * C::kPage + (p.kv_merged ? 0 : t_h * C::kHalf);
+                const int c1 = p.kv_merged ? 0 : slot_in_blk + 8 * t_h;
+                const int c3 = p.kv_merged ? blk_t * (p.BS >> 3) + (slot_in_blk >> 3) : g;
+                const int c4 = p.kv_merged ? g : blk_t;
+                if (mc)
+                    tma_load_5d_mc(dst, tmap, full_bar, 0, c1, 0, c3, c4, mc_mask, pol_last);
                 else
-                    tma_load_5d_mc(tile + t_pg * C::kPage + t_h * C::kHalf, tmap, full_bar, 0, slot_in_blk + 8 * t_h,
-                                   0, g, blk_t, mc_mask, pol_last);
+                    tma_load_5d(dst, tmap, full_bar, 0, c1, 0, c3, c4, pol_last);
             }
             const bool part = full_mask != 0xffu;
             if (part) {
@@ -457,6 +511,7 @@ __global__ void __launch_bounds__(384, 1)
             }
         }
         if (pend) retire(0);
+        if (n_it <= ring) cluster_wait();
         // Wait until both CTAs have released each slot for the last time
         // (forwarding this CTA's release): afterwards no arrival from the
         // other CTA is still travelling to this one.
@@ -470,6 +525,7 @@ __global__ void __launch_bounds__(384, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ bias windows
+        cluster_wait();
         // Band tile n's rel_logits, once every softmax warp has finished
         // reading band tile n-1's: one TMA box per token sub-box of TS tokens
         // (all G heads), rows of kBiasW distances from the 16-byte aligned
@@ -504,6 +560,7 @@ __global__ void __launch_bounds__(384, 1)
         __syncwarp();
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------ MMA issuer
+        cluster_wait();
         if (lane == 0 && n_it > 0) {
             constexpr uint32_t idS = umma_idesc_bf16(128, C::BN, false);
             constexpr uint32_t idPV = umma_idesc_bf16(128, D, true);
@@ -613,26 +670,16 @@ __global__ void __launch_bounds__(384, 1)
         float m_run = -CUDART_INF_F, l_half = 0.f;  // reference maximum (an integer in log2 units), half-row sum
         bool any_abort = false;
 
-        // Warps 4-7 copy the Q tile into TMEM: row r to lane r, bf16 pairs per
-        // column (zeros past the tile's rows).
+        // Warps 4-7 store the Q tile (loaded at the start) into TMEM: row r to
+        // lane r, bf16 pairs per column (zeros past the tile's rows).
         if (half == 0) {
-            uint32_t qv[D / 64][32];
-            const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.q) +
-                                                              (size_t)t * p.q_st + (size_t)h * p.q_sh);
-#pragma unroll
-            for (int c = 0; c < D / 8; ++c) {
-                const uint4 v = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-                qv[c / 8][4 * (c % 8)] = v.x;
-                qv[c / 8][4 * (c % 8) + 1] = v.y;
-                qv[c / 8][4 * (c % 8) + 2] = v.z;
-                qv[c / 8][4 * (c % 8) + 3] = v.w;
-            }
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) tmem_st32(lane_base + C::kQCol + 32 * c, qv[c]);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&bars->q_full);
         }
+        cluster_wait();
 
         // Bias windows (VEC): a band tile's rel_logits arrive by TMA as rows of
         // kBiasW values, one row per (token, head) of the tile, each starting at
@@ -938,7 +985,7 @@ LaunchShape prefill_shape(const AttnParams& p) {
     } else {
         s.grid = dim3((qtiles + kCluster - 1) / kCluster * kCluster, p.Hk, p.B * p.num_splits);
     }
-    s.block = 384;
+    s.block = PrefillCfg<128>::kThreads;
     s.smem = p.D == 128 ? prefill_smem_bytes<128>() : prefill_smem_bytes<64>();
     s.nstage = p.D == 128 ? PrefillCfg<128>::kStages : PrefillCfg<64>::kStages;
     return s;
