@@ -289,46 +289,6 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     // both of its CTAs leave at once (the same test in both).
     if (active == 0) return;
 
-    // Start-up latencies overlap the barrier and cluster set-up: warps 4-7
-    // load their query rows into registers (they go to TMEM once it is
-    // allocated), the producers their first block-table windows.
-    uint32_t qv[D / 64][32];
-    if (me_active && warp >= 4 && warp < 8) {
-        const int r = (warp & 3) * 32 + lane;
-        const bool valid = r < n_rows;
-        const int t = q0 + i0 + (valid ? r / G : 0), h = g * G + (valid ? r % G : 0);
-        const uint4* src =
-            reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.q) + (size_t)t * p.q_st + (size_t)h * p.q_sh);
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-            const uint4 v = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-            qv[c / 8][4 * (c % 8)] = v.x;
-            qv[c / 8][4 * (c % 8) + 1] = v.y;
-            qv[c / 8][4 * (c % 8) + 2] = v.z;
-            qv[c / 8][4 * (c % 8) + 3] = v.w;
-        }
-    }
-    // Block-table windows of 4 tiles: lane l holds the physical block of
-    // 16-key group l % 8 of tile w0 + l / 8; the next window is fetched one
-    // window ahead (32 consecutive entries when BS is 16).
-    const int32_t* bt = p.block_table + (size_t)b * p.bt_stride;
-    auto load_win = [&](int w0) -> int {
-        int v = 0;
-        const int jw = w0 + (lane >> 3);
-        if (jw < n_it) {
-            const int jg = key_block(jw) * C::BN + 16 * (lane & 7);
-            // (a key past the table's width, i.e. cache_seqlens > MB * BS,
-            // reads no entry: the clamp below then keeps block 0)
-            if (jg < sk && jg / p.BS < p.max_blocks) v = __ldg(bt + jg / p.BS);
-        }
-        return v;
-    };
-    int win_cur = 0, win_nxt = 0;
-    if (me_active && (warp == 0 || warp == 2)) {
-        win_cur = load_win(0);
-        win_nxt = load_win(4);
-    }
-
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, C::kSoftThreads / 2);
         for (int i = 0; i < C::kStages; ++i) {
@@ -352,6 +312,28 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         bars->abort = 0;
         fence_mbar_init();
     }
+    // The producers load their first block-table windows now: the first K
+    // and V boxes wait on them.  Block-table windows of 4 tiles: lane l holds
+    // the physical block of 16-key group l % 8 of tile w0 + l / 8; the next
+    // window is fetched one window ahead (32 consecutive entries when BS is 16).
+    const int32_t* bt = p.block_table + (size_t)b * p.bt_stride;
+    auto load_win = [&](int w0) -> int {
+        int v = 0;
+        const int jw = w0 + (lane >> 3);
+        if (jw < n_it) {
+            const int jg = key_block(jw) * C::BN + 16 * (lane & 7);
+            // (a key past the table's width, i.e. cache_seqlens > MB * BS,
+            // reads no entry: the clamp below then keeps block 0)
+            if (jg < sk && jg / p.BS < p.max_blocks) v = __ldg(bt + jg / p.BS);
+        }
+        return v;
+    };
+    int win_cur = 0, win_nxt = 0;
+    if (me_active && (warp == 0 || warp == 2)) {
+        win_cur = load_win(0);
+        win_nxt = load_win(4);
+    }
+
     if (me_active && warp == C::kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(&bars->tmem_base)),
@@ -670,9 +652,21 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
         float m_run = -CUDART_INF_F, l_half = 0.f;  // reference maximum (an integer in log2 units), half-row sum
         bool any_abort = false;
 
-        // Warps 4-7 store the Q tile (loaded at the start) into TMEM: row r to
-        // lane r, bf16 pairs per column (zeros past the tile's rows).
+        // Warps 4-7 copy the Q tile into TMEM: row r to lane r, bf16 pairs per
+        // column (zeros past the tile's rows).  The loads overlap the first K
+        // tile's flight (issued before the barrier the other warps wait at).
         if (half == 0) {
+            uint32_t qv[D / 64][32];
+            const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.q) +
+                                                              (size_t)t * p.q_st + (size_t)h * p.q_sh);
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) {
+                const uint4 v = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+                qv[c / 8][4 * (c % 8)] = v.x;
+                qv[c / 8][4 * (c % 8) + 1] = v.y;
+                qv[c / 8][4 * (c % 8) + 2] = v.z;
+                qv[c / 8][4 * (c % 8) + 3] = v.w;
+            }
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) tmem_st32(lane_base + C::kQCol + 32 * c, qv[c]);
             tmem_wait_st();
