@@ -99,7 +99,12 @@ typedef enum {
  *                  final bf16 rounding), caller-allocated; must not alias an input
  *   stream         the stream all work is ordered on
  *
- * Supported: D in {64, 128}; BS a multiple of 16; H % Hk == 0; H / Hk <= 128.
+ * Supported: D in {64, 128, 256}; BS a multiple of 16; H % Hk == 0;
+ * H / Hk <= 128.  Above 64 GQA-packed rows, D = 256 runs the CTA-pair prefill
+ * kernel (2-SM tcgen05 MMAs); D = 64 and 128 run the one-CTA prefill kernel
+ * (D = 128 on the CTA-pair kernel when the environment variable
+ * REL_ATTN_PREFILL_PAIR=1 is set and rel_logits are bf16 with R % 8 == 0 or
+ * absent).
  *
  * Ownership: every tensor is caller-owned device memory, borrowed until the
  * stream work completes.  When num_splits > 1 the library allocates a

@@ -178,6 +178,16 @@ def chunked_prefill(seed: int = 0, batch: int = 4, q_len: int = 4096, prefix: in
                      name="chunked_prefill")
 
 
+def chunked_prefill_d256(seed: int = 0, batch: int = 4, q_len: int = 4096, prefix: int = 4096) -> Case:
+    """The chunked-prefill shape at head_dim 256 (the CTA-pair prefill
+    kernel's size): 4 requests of 4096 query tokens on a 4096-token prefix,
+    32/8 heads, rel_extent 2048, rel_logits ~ N(0, 0.5^2), causal, one split."""
+    return make_case(seed=seed, seqlens_q=[q_len] * batch, seqlens_k=[prefix + q_len] * batch,
+                     num_heads=32, num_kv_heads=8, head_dim=256, block_size=16,
+                     rel_extent=2048, causal=True, rel_std=0.5, num_splits=1,
+                     name="chunked_prefill_d256")
+
+
 def mixed_window(seed: int = 0, batch: int = 32) -> Case:
     """32 requests, q lens log-uniform in [1, 2048], KV = prefix U[0, 32768] +
     q len, 32/8 heads, head_dim 128, window (4096, 0), rel_extent 512, causal."""
@@ -195,5 +205,6 @@ WORKLOADS = {
     "long_decode": long_decode,
     "batched_decode": batched_decode,
     "chunked_prefill": chunked_prefill,
+    "chunked_prefill_d256": chunked_prefill_d256,
     "mixed_window": mixed_window,
 }
