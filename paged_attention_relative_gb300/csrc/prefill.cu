@@ -419,10 +419,14 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
             if (lane == 0) mbar_arrive_remote(peer_bar0 + (uint32_t)(slot - ring0) * 8u);
             wait_slot(&bars->kv_peer[slot], par, kSitePrefillKEmpty);
         };
+        bool waited = false;  // this thread's cluster_wait is done
         for (int jj = 0; jj < n_it; ++jj) {
             // Multicast loads and releases to the other CTA from the second
             // use of a slot on.
-            if (jj == ring) cluster_wait();
+            if (jj == ring) {
+                cluster_wait();
+                waited = true;
+            }
             const bool mc = jj >= ring;
             const int slot = ring0 + sidx;
             wait_slot(&bars->kv_empty[slot], eph, kSitePrefillKEmpty);
@@ -493,7 +497,9 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
             }
         }
         if (pend) retire(0);
-        if (n_it <= ring) cluster_wait();
+        // (also when the loop stopped early on an abort: every thread waits
+        // once between its cluster arrivals)
+        if (!waited) cluster_wait();
         // Wait until both CTAs have released each slot for the last time
         // (forwarding this CTA's release): afterwards no arrival from the
         // other CTA is still travelling to this one.
