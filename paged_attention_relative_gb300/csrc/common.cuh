@@ -363,30 +363,35 @@ __device__ __forceinline__ void tma_load_3d_pair(void* dst, const void* desc, ui
         : "memory");
 }
 
-// 2-SM MMAs (cta_group::2): issued by one thread of the pair's even CTA; the
+// 2-SM MMAs (cta_group::2): issued by one warp of the pair's even CTA; the
 // M = 256 rows are the two CTAs' 128 TMEM lanes at the same column, and the
 // B operand is split by N, each CTA holding its half at the same shared
-// address.  A from shared memory (ss) or from TMEM (ts).
+// address.  A from shared memory (ss) or from TMEM (ts).  Like the 1-SM forms
+// below, the whole warp calls these converged and one lane chosen by
+// elect.sync issues.
 template <int ACC>
 __device__ __forceinline__ void umma2_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
-    asm volatile("tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, %4;" ::"r"(d_tmem), "l"(a_desc),
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, %4;\n\t}" ::"r"(d_tmem), "l"(a_desc),
                  "l"(b_desc), "r"(idesc), "n"(ACC)
                  : "memory");
 }
 
 template <int ACC>
 __device__ __forceinline__ void umma2_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc) {
-    asm volatile("tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, %4;" ::"r"(d_tmem), "r"(a_tmem),
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, %4;\n\t}" ::"r"(d_tmem), "r"(a_tmem),
                  "l"(b_desc), "r"(idesc), "n"(ACC)
                  : "memory");
 }
 
-// Arrive once on bar in both CTAs of the pair when every 2-SM MMA this
-// thread issued so far has completed.
+// Arrive once on bar in both CTAs of the pair when every 2-SM MMA the
+// issuing lane issued so far has completed (whole warp, converged).
 __device__ __forceinline__ void umma2_commit_both(uint64_t* bar) {
     asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+        "\n\t}" ::"r"(smem_u32(bar)),
         "h"((uint16_t)3)
         : "memory");
 }
@@ -446,56 +451,46 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, bool b_mn_m
            ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Same with the A operand read from TMEM (one row per lane, two 16-bit
-// elements per 32-bit column; a K step of 16 covers 8 columns).
-__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                                 uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Same two with a compile-time accumulate flag (no predicate set-up between
-// back-to-back MMAs).
+// 1-SM MMA, kind::f16 (bf16 A and B, fp32 accumulator), ACC = 0 overwrites D.
+// A from shared memory (ss) or from TMEM (ts: one row per lane, two 16-bit
+// elements per 32-bit column, a K step of 16 covers 8 columns).
+//
+// The whole warp calls these, converged, and the lane that elect.sync picks
+// issues.  Measured on GB300: one lane of a divergent `lane == 0` branch
+// needs ~50 cycles per MMA, so an N = 128 MMA (64 cycles of tensor work)
+// barely keeps the pipe fed and nothing else fits between two groups; the
+// elected form issues eight MMAs in ~110 cycles.
 template <int ACC>
 __device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
-    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, %4;" ::"r"(d_tmem), "l"(a_desc),
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, %4;\n\t}" ::"r"(d_tmem), "l"(a_desc),
                  "l"(b_desc), "r"(idesc), "n"(ACC)
                  : "memory");
 }
 
 template <int ACC>
 __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc) {
-    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, %4;" ::"r"(d_tmem), "r"(a_tmem),
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, %4;\n\t}" ::"r"(d_tmem), "r"(a_tmem),
                  "l"(b_desc), "r"(idesc), "n"(ACC)
                  : "memory");
 }
 
-// Arrive once on the mbarrier when every tcgen05 operation this thread issued
-// so far has completed.
+// Arrive once on the mbarrier when every tcgen05 operation the issuing lane
+// issued so far has completed (whole warp, converged; one elected lane).
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+                     smem_u32(bar))
                  : "memory");
 }
 
-// Arrive once on bar in every CTA of ctaMask when the prior MMAs complete.
-__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(mask)
-        : "memory");
+// mbar_wait for a whole warp: every lane waits, and all get the same answer
+// (a lane whose wait timed out makes the warp's answer false), so the warp
+// stays converged for the elected issue forms above.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint64_t timeout_ns, int site,
+                                               int* err) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, timeout_ns, site, err));
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }

@@ -35,27 +35,30 @@
 //              two window buffers (one with D = 64) once the softmax warps
 //              have released that buffer's previous fill (see below), so the
 //              next band tile's windows load while the current one is read.
-//   warp 3     MMA issuer (one thread) and TMEM owner: S_j = Q K_j^T into one
-//              of two TMEM buffers (M=128, N=128, K=head_dim, Q read from
-//              TMEM), then O += P_{j-1} V_{j-1} with P read from TMEM and V
-//              from shared memory (MN-major); tcgen05.commit signals
+//   warp 3     MMA issuer (the whole warp runs the loop, one elected lane
+//              issues) and TMEM owner.  Per tile and per key half h (keys
+//              [64h, 64h + 64)): S_h = Q K_j[64h..]^T (M=128, N=64,
+//              K=head_dim, Q read from TMEM) and O_h += P_h V_j[64h..] (P_h
+//              read from TMEM, V from shared memory, MN-major); the two
+//              halves are independent softmax streams, like two splits of
+//              the key range merged at the end.  tcgen05.commit signals
 //              completion.
-//   warps 4-11 softmax: warps 4-7 take keys [0, 64) of every tile and warps
-//              8-11 keys [64, 128); warp w reads TMEM lanes 32*(w%4).. so
-//              thread (w, lane) owns half of row 32*(w%4) + lane.  Per tile it
-//              reads its half of S_j, forms sc * q.k + bias (natural units;
-//              tiles outside every row's bias band keep the raw q.k and fold
-//              the scale into the exponent), masks only when some row of the
-//              warp does not see the whole half tile, publishes its half-row
-//              maximum to its partner through shared memory (an mbarrier per
-//              tile parity), computes its half of P_j against the current
-//              reference maximum while the partner's arrives, writes it into
-//              TMEM as bf16 pairs, rescales its half of the O row when the
-//              reference moved, and writes its half of the output.  The
-//              reference maximum is an integer in log2 units (so weights do
-//              not depend on the split partition, see kQuantC) and moves
-//              lazily (only when the row maximum exceeds it by more than
-//              2^8), so O is rarely rescaled.  The
+//   warps 4-11 softmax: warps 4-7 take key half 0 of every tile and warps
+//              8-11 half 1; warp w reads TMEM lanes 32*(w%4).. so thread
+//              (w, lane) owns half h of row 32*(w%4) + lane.  Per tile it
+//              reads S_h (and releases the buffer at once, so the next S_h
+//              computes during this tile's exponentials), forms sc * q.k +
+//              bias (natural units; tiles outside every row's bias band keep
+//              the raw q.k and fold the scale into the exponent), masks only
+//              when some row of the warp does not see the whole half tile,
+//              computes P_h against its half's reference maximum, writes it
+//              into TMEM as bf16 pairs and rescales its O_h row when the
+//              reference moved.  Each half keeps its own reference maximum,
+//              an integer in log2 units (so weights do not depend on the
+//              split partition, see kQuantC) that moves lazily (only when the
+//              half-row maximum exceeds it by more than 2^8), so no maxima
+//              cross between warps during the tiles.  The epilogue merges the
+//              halves by exact powers of two and writes the output.  The
 //              bias of a band tile is staged by warp 1: one 152-value window
 //              per (token, head) row, starting at the 16-byte aligned
 //              distance below the row's token sub-box, zero outside [0, R),
@@ -63,11 +66,9 @@
 // Every mbarrier wait is bounded; on timeout the kernel records the site in
 // the device error word and winds down.
 //
-// TMEM columns: S0 [0,128), S1 [128,256), O [256,256+D), Q [256+D,256+3D/2).
-// P_j overwrites the first half of each 64-column half of S_j's buffer once
-// the thread owning that half has read it (keys [0, 64) of the tile in
-// columns [0, 32), keys [64, 128) in [64, 96)).  Warps 4-7 copy Q into TMEM
-// at the start.
+// TMEM columns: O_0 [0,D), O_1 [D,2D), S_0 and S_1 (64 each), P_0 and P_1
+// (32 each: 64 keys as bf16 pairs), Q (D/2: bf16 pairs).  Warps 4-7 copy Q
+// into TMEM at the start.
 //
 // Semantics: vLLM API docs, inkling_fa4_rel_attention (paged varlen forward);
 // bias rule: prhub report on vLLM PR #48858, score_mod_rel_bias.
@@ -116,11 +117,17 @@ struct PrefillCfg {
     static constexpr int kBiasBytes = 128 * kBiasW * 2 + 16 * 128;
     // Band tiles' windows are double-buffered where shared memory allows.
     static constexpr int kBiasBufs = D == 128 ? 2 : 1;
-    static constexpr int kXchBytes = 3 * 2 * 128 * 4;  // half-row maxima (2 tile buffers), half-row sums
+    // Per half and row: the final reference maximum and sum (epilogue merge).
+    static constexpr int kXchBytes = 2 * 2 * 128 * 4;
     static constexpr int kData = kStages * kTileBytes + kBiasBufs * kBiasBytes + kXchBytes;
+    // TMEM columns: O_0, O_1 (D each), S_0, S_1 (64 each), P_0, P_1 (32 each:
+    // 64 keys as bf16 pairs), Q (D / 2: bf16 pairs).  Half h of the softmax
+    // (keys [64h, 64h + 64) of every tile) owns S_h, P_h and O_h.
     static constexpr int kTmemCols = 512;
-    static constexpr int kOCol = 256;      // O: D columns
-    static constexpr int kQCol = 256 + D;  // Q: D / 2 columns (bf16 pairs)
+    static constexpr int kOCol = 0;
+    static constexpr int kSCol = 2 * D;
+    static constexpr int kPCol = 2 * D + 128;
+    static constexpr int kQCol = 2 * D + 192;
 };
 
 struct PrefillBars {
@@ -128,9 +135,10 @@ struct PrefillBars {
     uint64_t kv_full[10];
     uint64_t kv_empty[10];   // this CTA's MMAs have read the slot's current use (a local commit)
     uint64_t kv_peer[10];    // the other CTA's MMAs have (its producer forwards its kv_empty)
-    uint64_t s_full[2];
-    uint64_t x_full[2];      // per tile parity: every softmax warp has published its half-row maxima
-    uint64_t o_done;   // one phase per PV tile (rescale waits, never more than one phase behind)
+    uint64_t s_full[2];  // per half, one phase per tile: S_h(jj) is in TMEM
+    uint64_t s_free1;    // one phase per tile: warps 8-11 have read S_1 (warps 4-7 use the K slot's barrier)
+    uint64_t p_full1;    // one phase per tile: P_1 is in TMEM (warps 4-7 use the V slot's barrier)
+    uint64_t o_done[2];  // per half, one phase per PV tile: PV_h has read P_h and added into O_h
     uint64_t o_final;  // single phase: every MMA of the CTA has completed
     uint64_t bias_full[2];   // per window buffer, one phase per fill: its rel_logits windows have landed
     uint64_t bias_empty[2];  // per window buffer, one phase per fill: every softmax warp has read them
@@ -211,7 +219,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sKV = smem;
     uint8_t* sBias = sKV + C::kStages * C::kTileBytes;
-    float* sXch = reinterpret_cast<float*>(sBias + C::kBiasBufs * C::kBiasBytes);  // [3 bufs][2 halves][128 rows]
+    float* sM = reinterpret_cast<float*>(sBias + C::kBiasBufs * C::kBiasBytes);  // [2 halves][128 rows]
+    float* sL = sM + 2 * 128;                                                      // [2 halves][128 rows]
     PrefillBars* bars = reinterpret_cast<PrefillBars*>(sBias + C::kBiasBufs * C::kBiasBytes + C::kXchBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -292,18 +301,21 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, C::kSoftThreads / 2);
         for (int i = 0; i < C::kStages; ++i) {
-            // producer lanes + the expect_tx arrival; a V slot also takes one
-            // arrival per softmax warp once P of its tile is in TMEM, so the
-            // MMA thread waits once before each PV
-            mbar_init(&bars->kv_full[i], i < C::kKRing ? 33 : 33 + C::kSoftThreads / 32);
+            // producer lanes + the expect_tx arrival, plus one arrival per
+            // warp of softmax half 0: a K slot's once that half has read the
+            // previous tile's S_0 (its buffer may be overwritten), a V slot's
+            // once P_0 of its tile is in TMEM.  The MMA thread then waits once
+            // before S_0 and once before PV_0.
+            mbar_init(&bars->kv_full[i], 33 + 4);
             mbar_init(&bars->kv_empty[i], 1);
             mbar_init(&bars->kv_peer[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->s_full[i], 1);
-            mbar_init(&bars->x_full[i], C::kSoftThreads / 32);
+            mbar_init(&bars->o_done[i], 1);
         }
-        mbar_init(&bars->o_done, 1);
+        mbar_init(&bars->s_free1, 4);
+        mbar_init(&bars->p_full1, 4);
         mbar_init(&bars->o_final, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->bias_full[i], 1);
@@ -549,67 +561,82 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------ MMA issuer
         cluster_wait();
-        if (lane == 0 && n_it > 0) {
-            constexpr uint32_t idS = umma_idesc_bf16(128, C::BN, false);
+        // The whole warp runs the loop (converged); one elected lane issues.
+        if (n_it > 0) {
+            constexpr uint32_t idS = umma_idesc_bf16(128, 64, false);
             constexpr uint32_t idPV = umma_idesc_bf16(128, D, true);
             const uint32_t aKV = smem_u32(sKV);
-            bool ok = mbar_wait(&bars->q_full, 0, p.timeout_ns, kSitePrefillLoadQ, p.err);
-            // Descriptors are formed before each wait, so the MMAs of a tile
-            // issue back to back (any instruction between two of them delays
-            // the tensor pipe).  A descriptor's low bits hold address / 16, so
-            // a byte offset inside shared memory adds offset / 16.
+            bool ok = mbar_wait_warp(&bars->q_full, 0, p.timeout_ns, kSitePrefillLoadQ, p.err);
+            // Descriptors are formed before each wait, so the MMAs of a group
+            // issue back to back.  A descriptor's low bits hold address / 16,
+            // so a byte offset inside shared memory adds offset / 16.  Keys
+            // [64h, 64h + 64) of a tile are its pages 4h .. 4h + 3.
             const uint64_t dK0 = umma_desc_sw128(aKV, 16, C::kHalf);
             const uint64_t dV0 = umma_desc_sw128(aKV, 1024, C::kHalf);
+            constexpr uint64_t kHalfK = (uint64_t)((4 * C::kPage) >> 4);
             const uint32_t aq = tmem + C::kQCol;
-            // P_t sits in S buffer t % 2: keys [64h, 64h + 64) in columns
-            // [64h, 64h + 32) of the buffer.  The MMAs of this thread run in
-            // issue order, so S_{t+2} = Q K^T, issued after PV_t, overwrites
-            // the buffer only once PV_t has read P_t.
+            // O_h += P_h(t) V_t[64h, 64h + 64): four K-steps of 16 keys.  Half
+            // 0's P is covered by the V slot's full barrier (it also counts the
+            // arrivals of warps 4-7), half 1's by p_full1.
             auto issue_pv = [&](int t) {
-                const int pb = t & 1;
                 const int slot = C::kKRing + t % C::kVRing;
                 const uint64_t dv = dV0 + (uint64_t)((slot * C::kTileBytes) >> 4);
                 uint64_t dV[C::BN / 16];
 #pragma unroll
                 for (int kk = 0; kk < C::BN / 16; ++kk) dV[kk] = dv + (uint64_t)((kk * C::kPage) >> 4);
-                const uint32_t pcol = tmem + pb * C::BN;
-                const uint32_t od = tmem + C::kOCol;
-                // V_t has landed and every softmax warp has written its part of P_t.
-                ok = ok && mbar_wait(&bars->kv_full[slot], (t / C::kVRing) & 1, p.timeout_ns, kSitePrefillPFull,
-                                     p.err);
+                const uint32_t o0 = tmem + C::kOCol, o1 = tmem + C::kOCol + D;
+                const uint32_t p0 = tmem + C::kPCol, p1 = tmem + C::kPCol + 32;
+                ok = ok && mbar_wait_warp(&bars->kv_full[slot], (t / C::kVRing) & 1, p.timeout_ns, kSitePrefillPFull,
+                                          p.err);
                 if (!ok) return;
                 tc_fence_after();
                 if (t > 0)
-                    umma_ts<1>(od, pcol, dV[0], idPV);
+                    umma_ts<1>(o0, p0, dV[0], idPV);
                 else
-                    umma_ts<0>(od, pcol, dV[0], idPV);
+                    umma_ts<0>(o0, p0, dV[0], idPV);
 #pragma unroll
-                for (int kk = 1; kk < C::BN / 16; ++kk)
-                    umma_ts<1>(od, pcol + 64 * (kk >> 2) + 8 * (kk & 3), dV[kk], idPV);
-                umma_commit(&bars->o_done);
+                for (int kk = 1; kk < 4; ++kk) umma_ts<1>(o0, p0 + 8 * kk, dV[kk], idPV);
+                umma_commit(&bars->o_done[0]);
+                ok = mbar_wait_warp(&bars->p_full1, t & 1, p.timeout_ns, kSitePrefillPFull, p.err);
+                if (!ok) return;
+                tc_fence_after();
+                if (t > 0)
+                    umma_ts<1>(o1, p1, dV[4], idPV);
+                else
+                    umma_ts<0>(o1, p1, dV[4], idPV);
+#pragma unroll
+                for (int kk = 1; kk < 4; ++kk) umma_ts<1>(o1, p1 + 8 * kk, dV[4 + kk], idPV);
+                umma_commit(&bars->o_done[1]);
                 umma_commit(&bars->kv_empty[slot]);
             };
-            // Tile jj's S buffer, K slot and V slot depend on jj % 2 only when
-            // both rings have two slots: unroll by two so every descriptor and
-            // TMEM address is a constant.
+            // S_h(jj) = Q K_jj[64h, 64h + 64)^T (N = 64).  S_0 waits on the K
+            // slot's full barrier, which also counts warps 4-7 having read
+            // S_0(jj - 1); S_1 waits on s_free1.  Tile jj's K slot depends on
+            // jj % 2 only when the K ring has two slots: unroll by two so the
+            // descriptors are constants.
             auto issue_s = [&](int jj, auto par) {
                 constexpr int P = decltype(par)::value;
-                constexpr int slot = C::kKRing == 2 ? P : 0;
                 const int slot_rt = C::kKRing == 2 ? P : jj % C::kKRing;
                 const uint64_t dk = dK0 + (uint64_t)((slot_rt * C::kTileBytes) >> 4);
                 uint64_t dK[D / 16];
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) dK[kk] = dk + (uint64_t)((((kk >> 2) * 1024) + (kk & 3) * 32) >> 4);
-                const uint32_t sd = tmem + P * C::BN;
-                (void)slot;
-                ok = ok && mbar_wait(&bars->kv_full[slot_rt], (jj / C::kKRing) & 1, p.timeout_ns, kSitePrefillKFull,
-                                     p.err);
+                const uint32_t s0 = tmem + C::kSCol, s1 = tmem + C::kSCol + 64;
+                ok = ok && mbar_wait_warp(&bars->kv_full[slot_rt], (jj / C::kKRing) & 1, p.timeout_ns,
+                                          kSitePrefillKFull, p.err);
                 if (!ok) return;
                 tc_fence_after();
-                umma_ts<0>(sd, aq, dK[0], idS);
+                umma_ts<0>(s0, aq, dK[0], idS);
 #pragma unroll
-                for (int kk = 1; kk < D / 16; ++kk) umma_ts<1>(sd, aq + 8 * kk, dK[kk], idS);
-                umma_commit(&bars->s_full[P]);
+                for (int kk = 1; kk < D / 16; ++kk) umma_ts<1>(s0, aq + 8 * kk, dK[kk], idS);
+                umma_commit(&bars->s_full[0]);
+                ok = mbar_wait_warp(&bars->s_free1, jj & 1, p.timeout_ns, kSitePrefillSFull, p.err);
+                if (!ok) return;
+                tc_fence_after();
+                umma_ts<0>(s1, aq, dK[0] + kHalfK, idS);
+#pragma unroll
+                for (int kk = 1; kk < D / 16; ++kk) umma_ts<1>(s1, aq + 8 * kk, dK[kk] + kHalfK, idS);
+                umma_commit(&bars->s_full[1]);
                 umma_commit(&bars->kv_empty[slot_rt]);
             };
             using I0 = std::integral_constant<int, 0>;
@@ -700,25 +727,37 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                                (((base_h - 1) >> 1) - 31);
         const uint32_t psel = ((base_h - 1) & 1) ? 0x5432u : 0x3210u;
         int nb = 0;  // band tiles consumed
+        bool s_ready = false;  // S_h of the next tile seen complete during this one
+        // This half's S, P and O in TMEM.  Its S buffer is free again once its
+        // four warps have read it: warps 4-7 say so on the next tile's K slot
+        // barrier (the MMA thread waits on that one before S_0 anyway), warps
+        // 8-11 on s_free1.  The first S needs no read, so arrive for it now.
+        const uint32_t s_addr = lane_base + C::kSCol + 64 * half;
+        const uint32_t p_addr = lane_base + C::kPCol + 32 * half;
+        const uint32_t o_addr = lane_base + C::kOCol + D * half;
+        if (n_it > 0 && lane == 0) mbar_arrive(half == 0 ? &bars->kv_full[0] : &bars->s_free1);
 
         for (int jj = 0; jj < n_it; ++jj) {
-            const int sb = jj & 1;
             const int j0 = key_block(jj) * C::BN;
             const int jh = j0 + kh;  // first key of this half
             const bool band = band_tile(j0);
-            bool my_abort = !mbar_wait(&bars->s_full[sb], (jj >> 1) & 1, p.timeout_ns, kSitePrefillSFull, p.err);
-            my_abort = __any_sync(0xffffffffu, my_abort || aborted(bars));
+            // S_h(jj)'s barrier was usually seen complete already, tested
+            // during the previous tile's exponentials (a wait on a completed
+            // barrier still costs ~100 cycles).
+            const bool my_abort =
+                (!s_ready && !mbar_wait(&bars->s_full[half], jj & 1, p.timeout_ns, kSitePrefillSFull, p.err)) ||
+                aborted(bars);
             float2 s[32];  // keys (kh + 2e, kh + 2e + 1) of the tile
             float mx = -CUDART_INF_F;
             // raw: s keeps q.k (no bias on this tile); the scale folds into
             // the exponent.  Otherwise s holds sc * q.k + bias.
             const bool raw = !band && pos_scale;
-            if (!my_abort) {
+            {
                 tc_fence_after();
                 {
                     uint32_t v0[32], v1[32];
-                    tmem_ld32(lane_base + sb * C::BN + kh, v0);
-                    tmem_ld32(lane_base + sb * C::BN + kh + 32, v1);
+                    tmem_ld32(s_addr, v0);
+                    tmem_ld32(s_addr + 32, v1);
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
@@ -727,6 +766,10 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                     }
                 }
                 tc_fence_before();
+                // S_h(jj) is in registers: the MMA thread may overwrite the buffer.
+                __syncwarp();
+                if (lane == 0 && jj + 1 < n_it)
+                    mbar_arrive(half == 0 ? &bars->kv_full[(jj + 1) % C::kKRing] : &bars->s_free1);
 
                 if (!raw) {
                     const float2 sc2 = make_float2(sc, sc);
@@ -786,24 +829,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                 mx = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]), fmaxf(mk[6], mk[7]));
                 if (raw) mx *= sc;
             }
-            if (my_abort) {
-                any_abort = true;
-                break;
-            }
             if (band) ++nb;
-            // Publish this half's maximum.  The partner's is needed only to
-            // confirm the reference maximum (or, before the first visible
-            // key, to set it), so the exponentials start from the current
-            // reference and are redone in the rare case that it moves.
-            const int xb = jj & 1;
-            sXch[(xb * 2 + half) * 128 + r] = mx;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->x_full[xb]);
-            auto row_max = [&]() -> float {
-                if (!mbar_wait(&bars->x_full[xb], (jj >> 1) & 1, p.timeout_ns, kSitePrefillXchg, p.err))
-                    bars->abort = 1;
-                return fmaxf(mx, sXch[(xb * 2 + (half ^ 1)) * 128 + r]);
-            };
             const float c1 = raw ? sl2 : kLog2e;
             uint32_t w[32];
             float rsum = 0.f;
@@ -827,80 +853,93 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
                 const float2 rs2 = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
                 rsum = rs2.x + rs2.y;
             };
-            // Lazy rescaling: the reference maximum m_run (an integer in log2
-            // units) only moves when the row maximum exceeds it by more than
-            // 8, so P stays below 2^8 and O is rescaled rarely (by an exact
-            // power of two); O / l is unchanged.
+            // Each half keeps its own reference maximum m_run (an integer in
+            // log2 units), so no maxima cross between warps.  It moves lazily:
+            // only when this half-row's maximum exceeds it by more than 8, so
+            // P stays below 2^8 and O_h is rescaled rarely (by an exact power
+            // of two).  The halves are merged in the epilogue.
             float m_use = m_run;
             bool grow = false;
+            const float hmx = mx * kLog2e;
             if (m_run == -CUDART_INF_F) {
-                m_use = ref_max(row_max() * kLog2e);
-                exp_pass(m_use);
-            } else {
-                exp_pass(m_run);
-                const float rmx = row_max() * kLog2e;
-                if (rmx > m_run + kLazyRescale) {
-                    grow = true;
-                    m_use = ref_max(rmx);
-                    exp_pass(m_use);
-                }
+                m_use = ref_max(hmx);
+            } else if (hmx > m_run + kLazyRescale) {
+                grow = true;
+                m_use = ref_max(hmx);
+            }
+            exp_pass(m_use);
+            s_ready = jj + 1 < n_it && mbar_test_wait(&bars->s_full[half], (jj + 1) & 1);
+            if (__any_sync(0xffffffffu, my_abort)) {
+                any_abort = true;
+                bars->abort = 1;
+                break;
             }
             const float alpha = grow ? exp2_int(m_run - m_use) : 1.f;
-            // This half of P_j over the S columns this thread has already read
-            // (PV_{j-2}, the last reader of the buffer, completed before S_j).
-            tmem_st32(lane_base + sb * C::BN + kh, w);
             l_half = l_half * alpha + rsum;
             m_run = m_use;
-
-            // Rescale this half of the O row when the reference maximum moved
+            // P_h(jj) goes where P_h(jj - 1) was: PV_h(jj - 1) must have read
+            // it (and, for a rescale, finished adding into O_h).
+            if (jj >= 1) {
+                if (!mbar_wait(&bars->o_done[half], (jj - 1) & 1, p.timeout_ns, kSitePrefillOFull, p.err))
+                    bars->abort = 1;
+                tc_fence_after();
+            }
+            // Rescale this thread's O_h row when its reference moved
             // (warp-collective TMEM access).
             if (jj >= 1 && __any_sync(0xffffffffu, grow)) {
-                if (!mbar_wait(&bars->o_done, (jj - 1) & 1, p.timeout_ns, kSitePrefillOFull, p.err)) bars->abort = 1;
-                tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
+                for (int c = 0; c < D / 32; ++c) {
                     uint32_t v[32];
-                    const uint32_t ta = lane_base + C::kOCol + half * (D / 2) + c * 32;
-                    tmem_ld32(ta, v);
+                    tmem_ld32(o_addr + c * 32, v);
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                    tmem_st32(ta, v);
+                    tmem_st32(o_addr + c * 32, v);
                 }
             }
+            tmem_st32(p_addr, w);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->kv_full[C::kKRing + jj % C::kVRing]);
+            if (lane == 0) mbar_arrive(half == 0 ? &bars->kv_full[C::kKRing + jj % C::kVRing] : &bars->p_full1);
         }
 
-        // Epilogue: O / l, with l the sum of the two halves' partial sums.
-        // (buffer 2: the partner may still read buffer (n_it - 1) % 2 of the last tile)
-        sXch[(4 + half) * 128 + r] = l_half;
+        // Epilogue: merge the halves, O = (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / l
+        // with m = max(m_0, m_1) and l the same combination of the half-row
+        // sums (exact powers of two).  Thread (row, half) writes output dims
+        // [half D/2, half D/2 + D/2).
+        sM[half * 128 + r] = m_run;
+        sL[half * 128 + r] = l_half;
         const bool failed = bar_or(1, C::kSoftThreads, any_abort || aborted(bars));
-        const float l_tot = sXch[4 * 128 + r] + sXch[5 * 128 + r];
+        const float m0 = sM[r], m1 = sM[128 + r];
+        const float m_row = fmaxf(m0, m1);
+        const float f0 = m0 == -CUDART_INF_F ? 0.f : exp2_int(m0 - m_row);
+        const float f1 = m1 == -CUDART_INF_F ? 0.f : exp2_int(m1 - m_row);
+        const float l_tot = sL[r] * f0 + sL[128 + r] * f1;
         const bool have = n_it > 0 && !failed;
         if (have) {
             if (!mbar_wait(&bars->o_final, 0, p.timeout_ns, kSitePrefillOFull, p.err)) bars->abort = 1;
             tc_fence_after();
         }
         const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
+        const float g0 = f0 * inv_l, g1 = f1 * inv_l;
         const bool partial = p.num_splits > 1;
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
             const int col = half * (D / 2) + c * 32;  // output dims [col, col + 32)
-            uint32_t v[32];
+            uint32_t v[32], u[32];
             if (have) {
                 tmem_ld32(lane_base + C::kOCol + col, v);
+                tmem_ld32(lane_base + C::kOCol + D + col, u);
                 tmem_wait_ld();
             } else {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] = 0u;
+                for (int e = 0; e < 32; ++e) v[e] = u[e] = 0u;
             }
             if (!valid) continue;
             float o[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(v[e]) * inv_l;
+            for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(v[e]) * g0 + __uint_as_float(u[e]) * g1;
             if (partial) {
                 float* dst = p.ws_o + (((size_t)split * p.T + t) * p.H + h) * D + col;
 #pragma unroll
@@ -925,10 +964,10 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 1)
             }
         }
         if (valid && partial && half == 0)
-            p.ws_lse[((size_t)split * p.T + t) * p.H + h] = l_tot > 0.f ? m_run + __log2f(l_tot) : -CUDART_INF_F;
+            p.ws_lse[((size_t)split * p.T + t) * p.H + h] = l_tot > 0.f ? m_row + __log2f(l_tot) : -CUDART_INF_F;
         if (valid && !partial && half == 0 && p.lse)
             p.lse[(size_t)t * p.lse_st + (size_t)h * p.lse_sh] =
-                l_tot > 0.f ? (m_run + __log2f(l_tot)) * kLn2 : -CUDART_INF_F;
+                l_tot > 0.f ? (m_row + __log2f(l_tot)) * kLn2 : -CUDART_INF_F;
     }
 
     tc_fence_before();

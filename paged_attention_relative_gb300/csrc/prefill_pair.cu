@@ -432,11 +432,12 @@ __global__ void __launch_bounds__(384, 1)
         __syncwarp();
     } else if (warp == 3) {
         // ------------------------------------------------------ MMA issuer (even CTA)
-        if (rank == 0 && lane == 0 && n_it > 0) {
+        // The whole warp runs the loop (converged); one elected lane issues.
+        if (rank == 0 && n_it > 0) {
             constexpr uint32_t idS = umma_idesc_bf16(256, C::BN, false);
             constexpr uint32_t idPV = umma_idesc_bf16(256, C::D, true);
             constexpr int KS = C::D / 16;  // K-steps of S
-            bool ok = mbar_wait(&bars->q_full, 0, p.timeout_ns, kSitePrefillLoadQ, p.err);
+            bool ok = mbar_wait_warp(&bars->q_full, 0, p.timeout_ns, kSitePrefillLoadQ, p.err);
             // Descriptors: Q (K-major, kDB dim blocks), K half (K-major), V half
             // (MN-major, kVB 64-dim blocks 16 KB apart).  A descriptor's low
             // bits hold address / 16, so a byte offset adds offset / 16.
@@ -454,7 +455,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                 for (int kk = 0; kk < KS; ++kk)
                     bK[kk] = dK0 + (uint64_t)((ks * C::kKBytes + (kk >> 2) * (64 * 128) + (kk & 3) * 32) >> 4);
-                ok = ok && mbar_wait(&bars->k_full[jj & 1], (uint32_t)((jj >> 1) & 1), p.timeout_ns,
+                ok = ok && mbar_wait_warp(&bars->k_full[jj & 1], (uint32_t)((jj >> 1) & 1), p.timeout_ns,
                                      kSitePrefillKFull, p.err);
                 if (!ok) return;
                 tc_fence_after();
@@ -466,16 +467,16 @@ __global__ void __launch_bounds__(384, 1)
             };
             // O += P_t V_t: P from S buffer t % 2 (keys [64 h, 64 h + 64) in
             // columns [64 h, 64 h + 32)), V from V slot t % 2.  The MMAs of this
-            // thread run in issue order, so S_{t+2}, issued after PV_t,
+            // warp (always its lowest lane, the one elect.sync picks) run in issue order, so S_{t+2}, issued after PV_t,
             // overwrites the buffer only once PV_t has read P_t.
             auto issue_pv = [&](int t) {
                 const int pb = t & 1, vs = t % C::kRing;
                 uint64_t bV[8];
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) bV[kk] = dV0 + (uint64_t)((vs * C::kVBytes + kk * 2048) >> 4);
-                ok = ok && mbar_wait(&bars->p_full[pb], (uint32_t)((t >> 1) & 1), p.timeout_ns, kSitePrefillPFull,
+                ok = ok && mbar_wait_warp(&bars->p_full[pb], (uint32_t)((t >> 1) & 1), p.timeout_ns, kSitePrefillPFull,
                                      p.err);
-                ok = ok && mbar_wait(&bars->v_full[t & 1], (uint32_t)((t >> 1) & 1), p.timeout_ns, kSitePrefillVFull,
+                ok = ok && mbar_wait_warp(&bars->v_full[t & 1], (uint32_t)((t >> 1) & 1), p.timeout_ns, kSitePrefillVFull,
                                      p.err);
                 if (!ok) return;
                 tc_fence_after();
