@@ -113,24 +113,6 @@ rel_attn_status make_rel_map(const rel_attn_tensor* t, int G, int ts, CUtensorMa
     return REL_ATTN_OK;
 }
 
-// Paged cache (NB, BS, Hk, D) as a 4-D TMA tensor, innermost first:
-// (D, Hk, BS, NB), box (64 dims, 1 head, 16 slots, 1 block), 128-byte swizzle.
-rel_attn_status make_cache_map(const rel_attn_tensor* t, CUtensorMap* map, const char* name) {
-    auto enc = encode_fn();
-    if (!enc) return fail(REL_ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    cuuint64_t dims[4] = {(cuuint64_t)t->shape[3], (cuuint64_t)t->shape[2], (cuuint64_t)t->shape[1],
-                          (cuuint64_t)t->shape[0]};
-    cuuint64_t strides[3] = {(cuuint64_t)t->stride[2] * 2, (cuuint64_t)t->stride[1] * 2,
-                             (cuuint64_t)t->stride[0] * 2};
-    cuuint32_t box[4] = {64, 1, 16, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t->data, dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(REL_ATTN_ERR_UNSUPPORTED, "%s: TMA descriptor rejected (CUresult %d)", name, (int)r);
-    return REL_ATTN_OK;
-}
-
 // Paged cache (NB, BS, Hk, D) as a 5-D TMA view whose box is one 16-key page
 // (or half of one) of one kv head with `dbox` 64-dim blocks, 128-byte swizzle.
 // A box lands as [8-key half][64-dim block][8 keys][64 dims]: the halves, the
@@ -585,16 +567,14 @@ rel_attn_status paged_varlen(
     const bool pair =
         prefill && (D == 256 || (D == 128 && (rel_extent == 0 || p.vec_bias) && prefill_pair_requested()));
     if (prefill) {
-        if (pair) {
-            if ((st = make_cache_map(key_cache, &maps[0], "key_cache"))) return st;
-            if ((st = make_cache_map(value_cache, &maps[1], "value_cache"))) return st;
-        } else {
-            // (K and V share strides, checked above.)
-            p.kv_merged = p.c_s0 == (int64_t)BS * p.c_s1 ? 1 : 0;
-            const int dbox = (int)(D / 64);
-            if ((st = make_page_map(key_cache, dbox, p.kv_merged != 0, &maps[0], "key_cache"))) return st;
-            if ((st = make_page_map(value_cache, dbox, p.kv_merged != 0, &maps[1], "value_cache"))) return st;
-        }
+        // Page views of the caches: one TMA box per 16-key page (two when the
+        // pages are not contiguous).  K and V share strides, checked above.
+        // The CTA-pair kernel stages half of every V tile's dims per CTA.
+        p.kv_merged = p.c_s0 == (int64_t)BS * p.c_s1 ? 1 : 0;
+        const int dbox = (int)(D / 64);
+        if ((st = make_page_map(key_cache, dbox, p.kv_merged != 0, &maps[0], "key_cache"))) return st;
+        if ((st = make_page_map(value_cache, pair ? dbox / 2 : dbox, p.kv_merged != 0, &maps[1], "value_cache")))
+            return st;
         // Tokens per rel_logits box: the largest divisor of the tile's 128 / G
         // tokens that is at most 8 (a box then never crosses the tile).
         const int tpt = (int)(128 / G);

@@ -343,14 +343,14 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     }
 }
 
-// 4-D TMA load issued by either CTA of a pair whose completion is signalled
+// 5-D TMA load issued by either CTA of a pair whose completion is signalled
 // on an mbarrier that may live in the peer CTA (shared::cluster address).
-__device__ __forceinline__ void tma_load_4d_pair(void* dst, const void* desc, uint32_t bar, int c0, int c1, int c2,
-                                                 int c3, uint64_t policy) {
+__device__ __forceinline__ void tma_load_5d_pair(void* dst, const void* desc, uint32_t bar, int c0, int c1, int c2,
+                                                 int c3, int c4, uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
+        "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "l"(policy)
         : "memory");
 }
 

@@ -76,11 +76,13 @@ int prefill_bias_window();
 cudaError_t launch_prefill(const AttnParams& p, const CUtensorMap* maps, const LaunchShape& shape,
                            cudaStream_t stream);
 
-// 2-SM tcgen05 prefill kernel (CTA pairs, cta_group::2) for head_dim 128 with
-// rel_logits staged by TMA (vec_bias) or no bias: clusters of two CTAs, each
-// holding two 128-row query tiles.  maps[0..2] as for launch_prefill; maps[3]
-// describes q as a 3-D TMA tensor (D, H, T) with a (64, G, 128 / G) box and
-// 128-byte swizzle.
+// 2-SM tcgen05 prefill kernel (CTA pairs, cta_group::2) for head_dim 256, and
+// 128 on request, with rel_logits staged by TMA (vec_bias) or no bias:
+// clusters of two CTAs holding two 128-row query tiles.  maps[0] as for
+// launch_prefill; maps[1] the same page view of value_cache with a box of
+// D / 128 dim blocks (each CTA stages half of the dims); maps[2] as for
+// launch_prefill; maps[3] describes q as a 3-D TMA tensor (D, H, T) with a
+// (64, G, 128 / G) box and 128-byte swizzle.
 LaunchShape prefill_pair_shape(const AttnParams& p);
 cudaError_t launch_prefill_pair(const AttnParams& p, const CUtensorMap* maps, const LaunchShape& shape,
                                 cudaStream_t stream);

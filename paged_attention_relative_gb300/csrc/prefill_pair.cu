@@ -26,15 +26,20 @@
 // Warp roles (384 threads per CTA):
 //   warp 0     the query tile (TMA, one box per 64-dim block), then this CTA's
 //              half of every K tile into a ring (2 slots, 1 for head_dim
-//              256): 2 KB boxes (16 keys x 64 dims)
-//              straight from the paged cache, zero-filling cp.async only
-//              for the 16-key group that straddles the cache length (keys
-//              inside the cache but outside a row's window are finite and
-//              masked by the softmax).
+//              256): one TMA box per 16-key page with every dim block (two
+//              8-key boxes when the cache's pages are not contiguous),
+//              straight from the paged cache through a 5-D page view,
+//              zero-filling cp.async only for the 16-key group that
+//              straddles the cache length (keys inside the cache but outside
+//              a row's window are finite and masked by the softmax).  The
+//              TMA unit's cost is mostly per box, so page boxes (4 K and 8 V
+//              boxes per tile instead of 2 KB boxes: 32 at head_dim 256) cut
+//              the staging time per tile.
 //   warp 1     bias windows: for each band tile one TMA box per 8-token
 //              sub-box into one of three (head_dim 256: two) window buffers,
 //              once the softmax has released that buffer's previous fill.
-//   warp 2     this CTA's half of every V tile into a ring like K's.
+//   warp 2     this CTA's half of every V tile (its D/2 dims of every page:
+//              one box per page) into a ring like K's.
 //   warp 3     TMEM (512 columns, allocated by the pair) and, in the even
 //              CTA, the MMA thread.
 //   warps 4-11 softmax as in the one-CTA kernel: thread (w, lane) owns keys
@@ -72,8 +77,15 @@ struct PairCfg {
     static constexpr int kDB = D / 64;                // 64-dim (128-byte) blocks
     static constexpr int kVB = D / 128;               // 64-dim blocks of this CTA's V half
     static constexpr int kQBytes = kDB * 128 * 128;   // the query tile: kDB blocks x 128 rows x 128 B
-    static constexpr int kKBytes = kDB * 64 * 128;    // this CTA's K half: kDB blocks x 64 keys x 128 B
-    static constexpr int kVBytes = kVB * 128 * 128;   // this CTA's V half: kVB blocks x 128 keys x 128 B
+    // This CTA's halves of a K and a V tile, page by page (16 keys), each
+    // page as one TMA box lands: [8-key half][64-dim block][8 keys][128 B].
+    // K: 4 pages with every dim block; V: 8 pages with kVB dim blocks.
+    static constexpr int kKHalf = kDB * 1024;
+    static constexpr int kKPage = 2 * kKHalf;
+    static constexpr int kVHalf = kVB * 1024;
+    static constexpr int kVPage = 2 * kVHalf;
+    static constexpr int kKBytes = 4 * kKPage;
+    static constexpr int kVBytes = 8 * kVPage;
     static constexpr int kRing = D == 128 ? 2 : 1;    // K and V ring slots
     static constexpr int kBiasW = 152;                // rel_logits values per staged row
     static constexpr int kBiasBytes = 128 * kBiasW * 2 + 16 * 128;
@@ -281,16 +293,18 @@ __global__ void __launch_bounds__(384, 1)
             }
             __syncwarp();
         }
-        // 16-key groups of a tile this CTA stages: K groups 4 rank .. 4 rank + 3
-        // (every dim block; layout [dim block][64 keys][128 B]), V groups
-        // 0 .. 7 (dim blocks kVB rank .. kVB rank + kVB - 1; layout
-        // [dim block][128 keys][128 B]).
+        // 16-key pages of a tile this CTA stages: K pages 4 rank .. 4 rank + 3
+        // (every dim block), V pages 0 .. 7 (dim blocks kVB rank .. kVB rank +
+        // kVB - 1); local page i at i * page_bytes, laid out as its TMA box
+        // lands: [8-key half][dim block][8 keys][128 B].
         const int g_first = is_v ? 0 : 4 * rank;
         const int n_groups = is_v ? 8 : 4;
-        const int n_db = is_v ? C::kVB : C::kDB;       // dim blocks per group this CTA stages
+        const int n_db = is_v ? C::kVB : C::kDB;       // dim blocks per page this CTA stages
         const int db_first = is_v ? C::kVB * rank : 0;
-        const int db_stride = is_v ? 128 * 128 : 64 * 128;  // bytes between dim blocks in a slot
+        const int page_bytes = is_v ? C::kVPage : C::kKPage;
         const int slot_bytes = is_v ? C::kVBytes : C::kKBytes;
+        // One box per page when the cache's pages are contiguous, else one per 8-key half.
+        const int nbox = p.kv_merged ? 1 : 2;
         uint8_t* ring = is_v ? sV : sK;
         uint32_t full_bar[2];
         for (int i = 0; i < 2; ++i)
@@ -347,20 +361,24 @@ __global__ void __launch_bounds__(384, 1)
                 if (jg + 16 <= sk) full_mask |= 1u << i;
             }
             uint8_t* tile = ring + slot * slot_bytes;
-            const int boxes = __popc(full_mask) * n_db;
-            if (lane == 0) mbar_expect_tx_cluster(full_bar[jj & 1], (uint32_t)boxes * 2048u);
+            if (lane == 0) mbar_expect_tx_cluster(full_bar[jj & 1], (uint32_t)(__popc(full_mask) * page_bytes));
             __syncwarp();
-            // TMA lanes: lane -> (local group lane / n_db, dim block lane % n_db),
-            // n_groups * n_db boxes (8 with head_dim 128, 16 with 256).
+            // TMA lanes: lane -> (local page lane / nbox, half lane % nbox),
+            // through the page view of the cache (5-D; see make_page_map).
             {
-                const int li = (lane / n_db) & (n_groups - 1);
-                const int dbl = lane % n_db;
+                const int li = (lane / nbox) & (n_groups - 1);
+                const int t_h = lane % nbox;
                 const int pg = g_first + li;
                 const int blk = min(max(__shfl_sync(0xffffffffu, win_cur, wl + pg), 0), p.NB - 1);
-                if (lane < n_groups * n_db && ((full_mask >> li) & 1)) {
-                    uint8_t* dst = tile + dbl * db_stride + (is_v ? pg : li) * 2048;
-                    tma_load_4d_pair(dst, tmap, full_bar[jj & 1], 64 * (db_first + dbl), g, (j0 + 16 * pg) % p.BS, blk,
-                                     pol_last);
+                if (lane < n_groups * nbox && ((full_mask >> li) & 1)) {
+                    const int slot_in_blk = (j0 + 16 * pg) % p.BS;
+                    // merged view (64, 8, D/64, NB * BS / 8, Hk): half-page blk * BS / 8 + slot / 8;
+                    // split view (64, BS, D/64, Hk, NB): slot, head, block.
+                    uint8_t* dst = tile + li * page_bytes + (p.kv_merged ? 0 : t_h * (page_bytes / 2));
+                    const int c1 = p.kv_merged ? 0 : slot_in_blk + 8 * t_h;
+                    const int c3 = p.kv_merged ? blk * (p.BS >> 3) + (slot_in_blk >> 3) : g;
+                    const int c4 = p.kv_merged ? g : blk;
+                    tma_load_5d_pair(dst, tmap, full_bar[jj & 1], 0, c1, db_first, c3, c4, pol_last);
                 }
             }
             const bool part = full_mask != (1u << n_groups) - 1;
@@ -379,8 +397,9 @@ __global__ void __launch_bounds__(384, 1)
                         const int row = (c >> 3) & 15, chunk = c & 7;
                         const bool valid = jg + row < sk;
                         const uint16_t* src = src0 + (long long)row * p.c_s1 + 64 * (db_first + dbl) + chunk * 8;
-                        const uint32_t dst = smem_u32(tile + dbl * db_stride + (is_v ? pg : i) * 2048) +
-                                             sw128_offset((uint32_t)row, (uint32_t)chunk);
+                        const uint32_t dst = smem_u32(tile + i * page_bytes + (row >> 3) * (page_bytes / 2) +
+                                                      dbl * 1024) +
+                                             sw128_offset((uint32_t)(row & 7), (uint32_t)chunk);
                         cp_async_16(dst, valid ? src : cache, valid ? 16u : 0u, pol_last);
                     }
                 }
@@ -442,8 +461,8 @@ __global__ void __launch_bounds__(384, 1)
             // (MN-major, kVB 64-dim blocks 16 KB apart).  A descriptor's low
             // bits hold address / 16, so a byte offset adds offset / 16.
             const uint64_t dQ = umma_desc_sw128(smem_u32(sQ), 16, 1024);
-            const uint64_t dK0 = umma_desc_sw128(smem_u32(sK), 16, 1024);
-            const uint64_t dV0 = umma_desc_sw128(smem_u32(sV), 128 * 128, 1024);
+            const uint64_t dK0 = umma_desc_sw128(smem_u32(sK), 16, C::kKHalf);
+            const uint64_t dV0 = umma_desc_sw128(smem_u32(sV), 1024, C::kVHalf);
             uint64_t aQ[KS];
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk)
@@ -454,7 +473,7 @@ __global__ void __launch_bounds__(384, 1)
                 uint64_t bK[KS];
 #pragma unroll
                 for (int kk = 0; kk < KS; ++kk)
-                    bK[kk] = dK0 + (uint64_t)((ks * C::kKBytes + (kk >> 2) * (64 * 128) + (kk & 3) * 32) >> 4);
+                    bK[kk] = dK0 + (uint64_t)((ks * C::kKBytes + (kk >> 2) * 1024 + (kk & 3) * 32) >> 4);
                 ok = ok && mbar_wait_warp(&bars->k_full[jj & 1], (uint32_t)((jj >> 1) & 1), p.timeout_ns,
                                      kSitePrefillKFull, p.err);
                 if (!ok) return;
@@ -473,7 +492,7 @@ __global__ void __launch_bounds__(384, 1)
                 const int pb = t & 1, vs = t % C::kRing;
                 uint64_t bV[8];
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) bV[kk] = dV0 + (uint64_t)((vs * C::kVBytes + kk * 2048) >> 4);
+                for (int kk = 0; kk < 8; ++kk) bV[kk] = dV0 + (uint64_t)((vs * C::kVBytes + kk * C::kVPage) >> 4);
                 ok = ok && mbar_wait_warp(&bars->p_full[pb], (uint32_t)((t >> 1) & 1), p.timeout_ns, kSitePrefillPFull,
                                      p.err);
                 ok = ok && mbar_wait_warp(&bars->v_full[t & 1], (uint32_t)((t >> 1) & 1), p.timeout_ns, kSitePrefillVFull,
