@@ -17,11 +17,11 @@
 // past the request still takes part (its half of K/V, its softmax) and
 // writes nothing.
 //
-// Per key tile j the MMA thread issues S_j = Q K_j^T into TMEM buffer j % 2
-// and then O += P_{j-1} V_{j-1}, so S_{j+1} is computed while the softmax of
-// tile j runs.  Its two commits per tile (multicast to both CTAs) also free
-// the ring slots: the K slot of tile j once S_j completed, the V slot once
-// PV_j completed.
+// Per key tile j the MMA thread issues S_j = Q K_j^T (head_dim 128: per key
+// half) and then O += P_{j-1} V_{j-1}, so S_{j+1} is computed while the
+// softmax of tile j runs.  Its commits (multicast to both CTAs) also free the
+// ring slots: the K slot of tile j once S_j completed, the V slot once PV_j
+// completed.
 //
 // Warp roles (384 threads per CTA):
 //   warp 0     the query tile (TMA, one box per 64-dim block), then this CTA's
@@ -42,16 +42,22 @@
 //              one box per page) into a ring like K's.
 //   warp 3     TMEM (512 columns, allocated by the pair) and, in the even
 //              CTA, the MMA thread.
-//   warps 4-11 softmax as in the one-CTA kernel: thread (w, lane) owns keys
-//              [64 h, 64 h + 64) of row 32 * (w % 4) + lane, h = (w - 4) / 4;
-//              scale, sheared bias (read reversed from the staged window),
-//              mask, half-row maxima exchanged through shared memory,
-//              exponentials against an integer reference maximum that moves
-//              lazily (see kQuantC), P into TMEM over the S columns already
-//              read, a rare rescale of O, the epilogue.
+//   warps 4-11 softmax: thread (w, lane) owns keys [64 h, 64 h + 64) of row
+//              32 * (w % 4) + lane, h = (w - 4) / 4; scale, sheared bias (read
+//              reversed from the staged window), mask, exponentials against
+//              an integer reference maximum that moves lazily (see kQuantC),
+//              P into TMEM, a rare rescale of O, the epilogue.  head_dim 128:
+//              as in the one-CTA kernel, each key half is an independent
+//              stream (own S, P, O and reference maximum; S released as soon
+//              as it is read; halves merged in the epilogue), the per-half S
+//              MMA (N = 64) reading each CTA's 32 keys from K pages 2r, 2r + 1
+//              (half 0) and 2r + 4, 2r + 5 (half 1).  head_dim 256: one O, the
+//              two warps of a row exchange half-row maxima through shared
+//              memory, and P is written over the S columns already read.
 //
-// TMEM columns: S_0 [0, 128), S_1 [128, 256), O [256, 256 + D).  P_j lies in S
-// buffer j % 2: keys [64 h, 64 h + 64) in columns [64 h, 64 h + 32).
+// TMEM columns (PairCfg): head_dim 128 O_0, O_1, S_0, S_1, P_0, P_1;
+// head_dim 256 S_0 [0, 128), S_1 [128, 256), O [256, 512), P_j in S buffer
+// j % 2 (keys [64 h, 64 h + 64) in columns [64 h, 64 h + 32)).
 // Every mbarrier wait is bounded; on timeout the kernel records the site in
 // the device error word and winds down.
 //
@@ -99,17 +105,31 @@ struct PairCfg {
     static constexpr int kData = kOffXch + kXchBytes;
     static constexpr int kThreads = 384;
     static constexpr int kTmemCols = 512;
-    static constexpr int kOCol = 256;
     static constexpr int kSoftWarps = 8;
+    // head_dim 128: the two key halves of every tile are independent softmax
+    // streams, each with its own S, P and O in TMEM (O_0 [0,128), O_1
+    // [128,256), S_0 [256,320), S_1 [320,384), P_0 [384,416), P_1 [416,448))
+    // and its own reference maximum, merged in the epilogue.  head_dim 256:
+    // no room for a second O, so S is double-buffered (S_0 [0,128), S_1
+    // [128,256)), P is written over S and one O takes [256, 512).
+    static constexpr bool kHalves = D == 128;
+    static constexpr int kOCol = kHalves ? 0 : 256;
+    static constexpr int kSCol = 256;
+    static constexpr int kPCol = 384;
 };
 
 struct PairBars {
     uint64_t q_full;            // even CTA: both CTAs' query tiles have landed
     uint64_t k_full[2];         // even CTA: K slot filled in both CTAs (one phase per fill)
     uint64_t v_full[2];         // even CTA: V slot filled in both CTAs (one phase per fill)
-    uint64_t p_full[2];         // even CTA: P in S buffer b written by both CTAs' softmax warps
-    uint64_t s_full[2];         // both: S_j of S buffer j % 2 computed (one phase per use)
-    uint64_t o_done[2];         // both: PV_j, j % 2, completed (one phase per use)
+    // head_dim 256: index = S buffer (one phase per use, every other tile);
+    // head_dim 128: index = key half (one phase per tile).
+    uint64_t p_full[2];         // even CTA: P written by both CTAs' softmax warps
+    uint64_t s_full[2];         // both: S computed
+    uint64_t o_done[2];         // both: PV completed
+    uint64_t s_free[2];         // even CTA, head_dim 128: both CTAs' warps of key half h have read S_h
+    uint64_t k_empty[2];        // both, head_dim 128: K slot's tile consumed by S_0 and S_1 (per use)
+    uint64_t v_empty[2];        // both, head_dim 128: V slot's tile consumed by PV_0 and PV_1 (per use)
     uint64_t x_full[2];         // this CTA: per tile parity, every softmax warp published its half-row maxima
     uint64_t o_final;           // both: every MMA of the item completed
     uint64_t bias_full[3];      // this CTA: window buffer filled (one phase per fill)
@@ -232,10 +252,14 @@ __global__ void __launch_bounds__(384, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->k_full[i], 2);
             mbar_init(&bars->v_full[i], 2);
-            mbar_init(&bars->p_full[i], 2 * C::kSoftWarps);  // one arrival per softmax warp, both CTAs
+            // one arrival per softmax warp of both CTAs (head_dim 128: per key half)
+            mbar_init(&bars->p_full[i], C::kHalves ? C::kSoftWarps : 2 * C::kSoftWarps);
             mbar_init(&bars->s_full[i], 1);
             mbar_init(&bars->o_done[i], 1);
             mbar_init(&bars->x_full[i], C::kSoftWarps);
+            mbar_init(&bars->s_free[i], C::kSoftWarps);
+            mbar_init(&bars->k_empty[i], 1);
+            mbar_init(&bars->v_empty[i], 1);
         }
         mbar_init(&bars->o_final, 1);
         for (int i = 0; i < C::kBiasBufs; ++i) {
@@ -297,7 +321,11 @@ __global__ void __launch_bounds__(384, 1)
         // (every dim block), V pages 0 .. 7 (dim blocks kVB rank .. kVB rank +
         // kVB - 1); local page i at i * page_bytes, laid out as its TMA box
         // lands: [8-key half][dim block][8 keys][128 B].
-        const int g_first = is_v ? 0 : 4 * rank;
+        // (head_dim 128: K pages 2 rank, 2 rank + 1, 2 rank + 4, 2 rank + 5,
+        // so that each key half's S = Q K^T, N = 64, finds its 32 keys per
+        // CTA in local pages 0-1 and 2-3.)
+        const int g_first = is_v ? 0 : (C::kHalves ? 2 * rank : 4 * rank);
+        auto page_of = [&](int li) { return g_first + li + (!is_v && C::kHalves ? 2 * (li >> 1) : 0); };
         const int n_groups = is_v ? 8 : 4;
         const int n_db = is_v ? C::kVB : C::kDB;       // dim blocks per page this CTA stages
         const int db_first = is_v ? C::kVB * rank : 0;
@@ -311,7 +339,12 @@ __global__ void __launch_bounds__(384, 1)
             full_bar[i] = mapa_shared(smem_u32(is_v ? &bars->v_full[i] : &bars->k_full[i]), 0);
         // The slot of tile jj is free again once S (K) or PV (V) of tile
         // jj - kRing, the tile it held, has completed (barrier (jj - kRing) % 2).
+        // (head_dim 128: the slot's own empty barrier, one phase per use.)
         uint64_t* free_bar[2] = {is_v ? &bars->o_done[0] : &bars->s_full[0], is_v ? &bars->o_done[1] : &bars->s_full[1]};
+        if (C::kHalves) {
+            free_bar[0] = is_v ? &bars->v_empty[0] : &bars->k_empty[0];
+            free_bar[1] = is_v ? &bars->v_empty[1] : &bars->k_empty[1];
+        }
         // At most one cp.async batch (the partial groups of a tile) is in
         // flight; it is retired (landed, proxy-fenced, one arrival with a
         // cluster-scope release on the even CTA's barrier, whose MMA reads
@@ -355,9 +388,9 @@ __global__ void __launch_bounds__(384, 1)
             }
             const int wl = (jj & 3) * 8;
             const int j0 = key_block(jj) * C::BN;
-            uint32_t full_mask = 0;  // bit i: group g_first + i fully visible (whole-box TMA)
+            uint32_t full_mask = 0;  // bit i: local page i fully visible (whole-box TMA)
             for (int i = 0; i < n_groups; ++i) {
-                const int jg = j0 + 16 * (g_first + i);
+                const int jg = j0 + 16 * page_of(i);
                 if (jg + 16 <= sk) full_mask |= 1u << i;
             }
             uint8_t* tile = ring + slot * slot_bytes;
@@ -368,7 +401,7 @@ __global__ void __launch_bounds__(384, 1)
             {
                 const int li = (lane / nbox) & (n_groups - 1);
                 const int t_h = lane % nbox;
-                const int pg = g_first + li;
+                const int pg = page_of(li);
                 const int blk = min(max(__shfl_sync(0xffffffffu, win_cur, wl + pg), 0), p.NB - 1);
                 if (lane < n_groups * nbox && ((full_mask >> li) & 1)) {
                     const int slot_in_blk = (j0 + 16 * pg) % p.BS;
@@ -387,7 +420,7 @@ __global__ void __launch_bounds__(384, 1)
                 // n_db dim blocks x 16 keys x 8 chunks each.
                 for (int i = 0; i < n_groups; ++i) {
                     if ((full_mask >> i) & 1) continue;
-                    const int pg = g_first + i;
+                    const int pg = page_of(i);
                     const int jg = j0 + 16 * pg;
                     const int blk = min(max(__shfl_sync(0xffffffffu, win_cur, wl + pg), 0), p.NB - 1);
                     const uint16_t* src0 =
@@ -467,52 +500,116 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk)
                 aQ[kk] = dQ + (uint64_t)(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
-            // S_jj = Q K^T into S buffer jj % 2, K from ring slot jj % kRing.
-            auto issue_s = [&](int jj) {
-                const int sb = jj & 1, ks = jj % C::kRing;
-                uint64_t bK[KS];
+            if constexpr (C::kHalves) {
+                // Key half h of tile jj: S_h = Q K_jj[64h, 64h + 64)^T (N = 64:
+                // each CTA's 32 keys in its local pages 2h, 2h + 1) once both
+                // CTAs' warps of half h have read S_h(jj - 1) (s_free[h]); then
+                // O_h += P_h V_jj[64h, 64h + 64) (4 K-steps) once both CTAs
+                // wrote P_h (p_full[h]).  The slot's empty barrier follows the
+                // second half.
+                constexpr uint32_t idS2 = umma_idesc_bf16(256, 64, false);
+                auto issue_s = [&](int jj) {
+                    const int ks = jj % C::kRing;
+                    uint64_t bK[KS];
 #pragma unroll
-                for (int kk = 0; kk < KS; ++kk)
-                    bK[kk] = dK0 + (uint64_t)((ks * C::kKBytes + (kk >> 2) * 1024 + (kk & 3) * 32) >> 4);
-                ok = ok && mbar_wait_warp(&bars->k_full[jj & 1], (uint32_t)((jj >> 1) & 1), p.timeout_ns,
-                                     kSitePrefillKFull, p.err);
-                if (!ok) return;
-                tc_fence_after();
-                const uint32_t sd = tmem + sb * C::BN;
-                umma2_ss<0>(sd, aQ[0], bK[0], idS);
+                    for (int kk = 0; kk < KS; ++kk)
+                        bK[kk] = dK0 + (uint64_t)((ks * C::kKBytes + (kk >> 2) * 1024 + (kk & 3) * 32) >> 4);
+                    ok = ok && mbar_wait_warp(&bars->k_full[jj & 1], (uint32_t)((jj >> 1) & 1), p.timeout_ns,
+                                              kSitePrefillKFull, p.err);
 #pragma unroll
-                for (int kk = 1; kk < KS; ++kk) umma2_ss<1>(sd, aQ[kk], bK[kk], idS);
-                umma2_commit_both(&bars->s_full[sb]);
-            };
-            // O += P_t V_t: P from S buffer t % 2 (keys [64 h, 64 h + 64) in
-            // columns [64 h, 64 h + 32)), V from V slot t % 2.  The MMAs of this
-            // warp (always its lowest lane, the one elect.sync picks) run in issue order, so S_{t+2}, issued after PV_t,
-            // overwrites the buffer only once PV_t has read P_t.
-            auto issue_pv = [&](int t) {
-                const int pb = t & 1, vs = t % C::kRing;
-                uint64_t bV[8];
+                    for (int hh = 0; hh < 2; ++hh) {
+                        ok = ok && mbar_wait_warp(&bars->s_free[hh], (uint32_t)(jj & 1), p.timeout_ns,
+                                                  kSitePrefillSFull, p.err);
+                        if (!ok) return;
+                        tc_fence_after();
+                        const uint32_t sd = tmem + C::kSCol + 64 * hh;
+                        const uint64_t ho = (uint64_t)((2 * hh * C::kKPage) >> 4);
+                        umma2_ss<0>(sd, aQ[0], bK[0] + ho, idS2);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) bV[kk] = dV0 + (uint64_t)((vs * C::kVBytes + kk * C::kVPage) >> 4);
-                ok = ok && mbar_wait_warp(&bars->p_full[pb], (uint32_t)((t >> 1) & 1), p.timeout_ns, kSitePrefillPFull,
-                                     p.err);
-                ok = ok && mbar_wait_warp(&bars->v_full[t & 1], (uint32_t)((t >> 1) & 1), p.timeout_ns, kSitePrefillVFull,
-                                     p.err);
-                if (!ok) return;
-                tc_fence_after();
-                const uint32_t pcol = tmem + pb * C::BN, od = tmem + C::kOCol;
-                if (t > 0)
-                    umma2_ts<1>(od, pcol, bV[0], idPV);
-                else
-                    umma2_ts<0>(od, pcol, bV[0], idPV);
+                        for (int kk = 1; kk < KS; ++kk) umma2_ss<1>(sd, aQ[kk], bK[kk] + ho, idS2);
+                        umma2_commit_both(&bars->s_full[hh]);
+                    }
+                    umma2_commit_both(&bars->k_empty[ks]);
+                };
+                auto issue_pv = [&](int t) {
+                    const int vs = t % C::kRing;
+                    uint64_t bV[8];
 #pragma unroll
-                for (int kk = 1; kk < 8; ++kk) umma2_ts<1>(od, pcol + 64 * (kk >> 2) + 8 * (kk & 3), bV[kk], idPV);
-                umma2_commit_both(&bars->o_done[pb]);
-            };
-            for (int jj = 0; jj < n_it && ok; ++jj) {
-                issue_s(jj);
-                if (ok && jj >= 1) issue_pv(jj - 1);
+                    for (int kk = 0; kk < 8; ++kk)
+                        bV[kk] = dV0 + (uint64_t)((vs * C::kVBytes + kk * C::kVPage) >> 4);
+                    ok = ok && mbar_wait_warp(&bars->v_full[t & 1], (uint32_t)((t >> 1) & 1), p.timeout_ns,
+                                              kSitePrefillVFull, p.err);
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        ok = ok && mbar_wait_warp(&bars->p_full[hh], (uint32_t)(t & 1), p.timeout_ns,
+                                                  kSitePrefillPFull, p.err);
+                        if (!ok) return;
+                        tc_fence_after();
+                        const uint32_t od = tmem + C::kOCol + 128 * hh, pc = tmem + C::kPCol + 32 * hh;
+                        if (t > 0)
+                            umma2_ts<1>(od, pc, bV[4 * hh], idPV);
+                        else
+                            umma2_ts<0>(od, pc, bV[4 * hh], idPV);
+#pragma unroll
+                        for (int kk = 1; kk < 4; ++kk) umma2_ts<1>(od, pc + 8 * kk, bV[4 * hh + kk], idPV);
+                        umma2_commit_both(&bars->o_done[hh]);
+                    }
+                    umma2_commit_both(&bars->v_empty[vs]);
+                };
+                for (int jj = 0; jj < n_it && ok; ++jj) {
+                    issue_s(jj);
+                    if (ok && jj >= 1) issue_pv(jj - 1);
+                }
+                if (ok) issue_pv(n_it - 1);
+            } else {
+                // S_jj = Q K^T into S buffer jj % 2, K from ring slot jj % kRing.
+                auto issue_s = [&](int jj) {
+                    const int sb = jj & 1, ks = jj % C::kRing;
+                    uint64_t bK[KS];
+#pragma unroll
+                    for (int kk = 0; kk < KS; ++kk)
+                        bK[kk] = dK0 + (uint64_t)((ks * C::kKBytes + (kk >> 2) * 1024 + (kk & 3) * 32) >> 4);
+                    ok = ok && mbar_wait_warp(&bars->k_full[jj & 1], (uint32_t)((jj >> 1) & 1), p.timeout_ns,
+                                         kSitePrefillKFull, p.err);
+                    if (!ok) return;
+                    tc_fence_after();
+                    const uint32_t sd = tmem + sb * C::BN;
+                    umma2_ss<0>(sd, aQ[0], bK[0], idS);
+#pragma unroll
+                    for (int kk = 1; kk < KS; ++kk) umma2_ss<1>(sd, aQ[kk], bK[kk], idS);
+                    umma2_commit_both(&bars->s_full[sb]);
+                };
+                // O += P_t V_t: P from S buffer t % 2 (keys [64 h, 64 h + 64) in
+                // columns [64 h, 64 h + 32)), V from V slot t % 2.  The MMAs of
+                // this warp (always its lowest lane, the one elect.sync picks)
+                // run in issue order, so S_{t+2}, issued after PV_t, overwrites
+                // the buffer only once PV_t has read P_t.
+                auto issue_pv = [&](int t) {
+                    const int pb = t & 1, vs = t % C::kRing;
+                    uint64_t bV[8];
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) bV[kk] = dV0 + (uint64_t)((vs * C::kVBytes + kk * C::kVPage) >> 4);
+                    ok = ok && mbar_wait_warp(&bars->p_full[pb], (uint32_t)((t >> 1) & 1), p.timeout_ns, kSitePrefillPFull,
+                                         p.err);
+                    ok = ok && mbar_wait_warp(&bars->v_full[t & 1], (uint32_t)((t >> 1) & 1), p.timeout_ns, kSitePrefillVFull,
+                                         p.err);
+                    if (!ok) return;
+                    tc_fence_after();
+                    const uint32_t pcol = tmem + pb * C::BN, od = tmem + C::kOCol;
+                    if (t > 0)
+                        umma2_ts<1>(od, pcol, bV[0], idPV);
+                    else
+                        umma2_ts<0>(od, pcol, bV[0], idPV);
+#pragma unroll
+                    for (int kk = 1; kk < 8; ++kk) umma2_ts<1>(od, pcol + 64 * (kk >> 2) + 8 * (kk & 3), bV[kk], idPV);
+                    umma2_commit_both(&bars->o_done[pb]);
+                };
+                for (int jj = 0; jj < n_it && ok; ++jj) {
+                    issue_s(jj);
+                    if (ok && jj >= 1) issue_pv(jj - 1);
+                }
+                if (ok) issue_pv(n_it - 1);
             }
-            if (ok) issue_pv(n_it - 1);
             // The epilogue may be two or more o_done phases behind, where a
             // parity wait cannot tell phases apart: it has its own barrier.
             umma2_commit_both(&bars->o_final);
@@ -564,234 +661,466 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t psel = ((base_h - 1) & 1) ? 0x5432u : 0x3210u;
         int nb = 0;  // band tiles consumed
 
-        for (int jj = 0; jj < n_it; ++jj) {
-            const int sb = jj & 1;
-            const int j0 = key_block(jj) * C::BN;
-            const int jh = j0 + kh;  // first key of this half
-            const bool band = band_tile(j0);
-            bool my_abort = !mbar_wait(&bars->s_full[sb], (uint32_t)((jj >> 1) & 1), p.timeout_ns, kSitePrefillSFull,
-                                       p.err);
-            my_abort = __any_sync(0xffffffffu, my_abort || aborted(bars));
-            float2 s[32];  // keys (kh + 2e, kh + 2e + 1) of the tile
-            float mx = -CUDART_INF_F;
-            // raw: s keeps q.k (no bias on this tile); the scale folds into
-            // the exponent.  Otherwise s holds sc * q.k + bias.
-            const bool raw = !band && pos_scale;
-            if (!my_abort) {
-                tc_fence_after();
+        if constexpr (C::kHalves) {
+            // head_dim 128: key half `half` is its own softmax stream (S_h, P_h,
+            // O_h, reference maximum); its S buffer is released to the MMA
+            // thread (s_free, both CTAs' warps) as soon as it is read, so the
+            // next S_h computes during this tile's exponentials.
+            const uint32_t s_addr = lane_base + C::kSCol + 64 * half;
+            const uint32_t p_addr = lane_base + C::kPCol + 32 * half;
+            const uint32_t o_addr = lane_base + C::kOCol + 128 * half;
+            const uint32_t sfree_bar = mapa_shared(smem_u32(&bars->s_free[half]), 0);
+            bool s_ready = false;  // S_h of the next tile seen complete during this one
+            // The first S_h needs no read: arrive for it now.
+            if (n_it > 0 && lane == 0) mbar_arrive_remote(sfree_bar);
+            for (int jj = 0; jj < n_it; ++jj) {
+                const int j0 = key_block(jj) * C::BN;
+                const int jh = j0 + kh;  // first key of this half
+                const bool band = band_tile(j0);
+                const bool my_abort = (!s_ready && !mbar_wait(&bars->s_full[half], (uint32_t)(jj & 1), p.timeout_ns,
+                                                              kSitePrefillSFull, p.err)) ||
+                                      aborted(bars);
+                float2 s[32];  // keys (kh + 2e, kh + 2e + 1) of the tile
+                float mx = -CUDART_INF_F;
+                const bool raw = !band && pos_scale;
                 {
-                    uint32_t v0[32], v1[32];
-                    tmem_ld32(lane_base + sb * C::BN + kh, v0);
-                    tmem_ld32(lane_base + sb * C::BN + kh + 32, v1);
-                    tmem_wait_ld();
+                    tc_fence_after();
+                    {
+                        uint32_t v0[32], v1[32];
+                        tmem_ld32(s_addr, v0);
+                        tmem_ld32(s_addr + 32, v1);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        s[e] = make_float2(__uint_as_float(v0[2 * e]), __uint_as_float(v0[2 * e + 1]));
-                        s[16 + e] = make_float2(__uint_as_float(v1[2 * e]), __uint_as_float(v1[2 * e + 1]));
+                        for (int e = 0; e < 16; ++e) {
+                            s[e] = make_float2(__uint_as_float(v0[2 * e]), __uint_as_float(v0[2 * e + 1]));
+                            s[16 + e] = make_float2(__uint_as_float(v1[2 * e]), __uint_as_float(v1[2 * e + 1]));
+                        }
                     }
-                }
-                tc_fence_before();
-                if (!raw) {
-                    const float2 sc2 = make_float2(sc, sc);
-                    if (band && p.vec_bias) {
-                        const int bb = nb % C::kBiasBufs;
-                        if (!mbar_wait(&bars->bias_full[bb], (uint32_t)((nb / C::kBiasBufs) & 1), p.timeout_ns,
-                                       kSitePrefillRelFull, p.err))
-                            bars->abort = 1;
-                        const uint32_t* wb = wrow + bb * (C::kBiasBytes / 4);
-                        uint32_t wv[33];
+                    tc_fence_before();
+                    // S_h(jj) is in registers: the MMA thread may overwrite the buffer.
+                    __syncwarp();
+                    if (lane == 0 && jj + 1 < n_it) mbar_arrive_remote(sfree_bar);
+                    if (!raw) {
+                        const float2 sc2 = make_float2(sc, sc);
+                        if (band && p.vec_bias) {
+                            const int bb = nb % C::kBiasBufs;
+                            if (!mbar_wait(&bars->bias_full[bb], (uint32_t)((nb / C::kBiasBufs) & 1), p.timeout_ns,
+                                           kSitePrefillRelFull, p.err))
+                                bars->abort = 1;
+                            const uint32_t* wb = wrow + bb * (C::kBiasBytes / 4);
+                            uint32_t wv[33];
 #pragma unroll
-                        for (int i = 0; i < 33; ++i) wv[i] = wb[i];
+                            for (int i = 0; i < 33; ++i) wv[i] = wb[i];
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) {
+                                const uint32_t pr = __byte_perm(wv[31 - e], wv[32 - e], psel);
+                                s[e] = __ffma2_rn(
+                                    s[e], sc2, make_float2(__uint_as_float(pr & 0xffff0000u), __uint_as_float(pr << 16)));
+                            }
+                            // Every read of this band tile's windows is done.
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&bars->bias_empty[bb]);
+                        } else if (band) {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) {
+                                const int d = pos - (jh + 2 * e);
+                                const float b0 = valid && d >= 0 && d < R ? rel_at(p.rel, bias_f32, rel_row + d) : 0.f;
+                                const float b1 =
+                                    valid && d - 1 >= 0 && d - 1 < R ? rel_at(p.rel, bias_f32, rel_row + d - 1) : 0.f;
+                                s[e] = __ffma2_rn(s[e], sc2, make_float2(b0, b1));
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) s[e] = __fmul2_rn(s[e], sc2);
+                        }
+                    }
+                    // Mask (warp-uniform skip when every row of the warp sees the whole half tile).
+                    const bool row_full = !valid || (jh >= klo && jh + 64 <= khi);
+                    if (!__all_sync(0xffffffffu, row_full)) {
 #pragma unroll
                         for (int e = 0; e < 32; ++e) {
-                            const uint32_t pr = __byte_perm(wv[31 - e], wv[32 - e], psel);
-                            s[e] = __ffma2_rn(s[e], sc2,
-                                              make_float2(__uint_as_float(pr & 0xffff0000u), __uint_as_float(pr << 16)));
+                            const int j = jh + 2 * e;
+                            if (!row_full && !(j >= klo && j < khi)) s[e].x = -CUDART_INF_F;
+                            if (!row_full && !(j + 1 >= klo && j + 1 < khi)) s[e].y = -CUDART_INF_F;
                         }
-                        // Every read of this band tile's windows is done.
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&bars->bias_empty[bb]);
-                    } else if (band) {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const int d = pos - (jh + 2 * e);
-                            const float b0 = valid && d >= 0 && d < R ? rel_at(p.rel, bias_f32, rel_row + d) : 0.f;
-                            const float b1 =
-                                valid && d - 1 >= 0 && d - 1 < R ? rel_at(p.rel, bias_f32, rel_row + d - 1) : 0.f;
-                            s[e] = __ffma2_rn(s[e], sc2, make_float2(b0, b1));
-                        }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) s[e] = __fmul2_rn(s[e], sc2);
                     }
+                    float mk[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mk[i] = fmax3(s[i].x, s[i].y, s[8 + i].x);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mk[i] = fmax3(mk[i], s[8 + i].y, s[16 + i].x);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mk[i] = fmax3(mk[i], s[16 + i].y, s[24 + i].x);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mk[i] = fmaxf(mk[i], s[24 + i].y);
+                    mx = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]), fmaxf(mk[6], mk[7]));
+                    if (raw) mx *= sc;
                 }
-                // Mask (warp-uniform skip when every row of the warp sees the whole half tile).
-                const bool row_full = !valid || (jh >= klo && jh + 64 <= khi);
-                if (!__all_sync(0xffffffffu, row_full)) {
+                if (band && p.vec_bias) ++nb;
+                const float c1 = raw ? sl2 : kLog2e;
+                uint32_t w[32];
+                float rsum = 0.f;
+                // This half of P (bf16 pairs) and its row sum against the
+                // integer reference m: 2^(q(s * c1) - m), see kQuantC.
+                auto exp_pass = [&](float m) {
+                    const float offs = kQuantC + (m == -CUDART_INF_F ? 0.f : m);
+                    const float2 c12 = make_float2(c1, c1), qc = make_float2(kQuantC, kQuantC),
+                                 noff = make_float2(-offs, -offs);
+                    float2 rs[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) rs[i] = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
-                        const int j = jh + 2 * e;
-                        if (!row_full && !(j >= klo && j < khi)) s[e].x = -CUDART_INF_F;
-                        if (!row_full && !(j + 1 >= klo && j + 1 < khi)) s[e].y = -CUDART_INF_F;
+                        const float2 x = __fadd2_rn(__ffma2_rn(s[e], c12, qc), noff);
+                        const float2 pe = make_float2(ex2(x.x), ex2(x.y));
+                        rs[e & 3] = __fadd2_rn(rs[e & 3], pe);
+                        w[e] = pack_bf16(pe.x, pe.y);
+                    }
+                    const float2 rs2 = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
+                    rsum = rs2.x + rs2.y;
+                };
+                // This half's reference maximum moves lazily (only when its
+                // maximum exceeds it by more than 8 in log2 units).
+                float m_use = m_run;
+                bool grow = false;
+                const float hmx = mx * kLog2e;
+                if (m_run == -CUDART_INF_F) {
+                    m_use = ref_max(hmx);
+                } else if (hmx > m_run + kLazyRescale) {
+                    grow = true;
+                    m_use = ref_max(hmx);
+                }
+                exp_pass(m_use);
+                s_ready = jj + 1 < n_it && mbar_test_wait(&bars->s_full[half], (uint32_t)((jj + 1) & 1));
+                if (__any_sync(0xffffffffu, my_abort)) {
+                    any_abort = true;
+                    bars->abort = 1;
+                    break;
+                }
+                const float alpha = grow ? exp2_int(m_run - m_use) : 1.f;
+                l_half = l_half * alpha + rsum;
+                m_run = m_use;
+                // P_h goes where P_h of the previous tile was: its PV_h must
+                // have completed (and, for a rescale, finished adding into O_h).
+                if (jj >= 1) {
+                    if (!mbar_wait(&bars->o_done[half], (uint32_t)((jj - 1) & 1), p.timeout_ns, kSitePrefillOFull,
+                                   p.err))
+                        bars->abort = 1;
+                    tc_fence_after();
+                }
+                if (jj >= 1 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t v[32];
+                        tmem_ld32(o_addr + c * 32, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                        tmem_st32(o_addr + c * 32, v);
                     }
                 }
-                float mk[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mk[i] = fmax3(s[i].x, s[i].y, s[8 + i].x);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mk[i] = fmax3(mk[i], s[8 + i].y, s[16 + i].x);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mk[i] = fmax3(mk[i], s[16 + i].y, s[24 + i].x);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mk[i] = fmaxf(mk[i], s[24 + i].y);
-                mx = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]), fmaxf(mk[6], mk[7]));
-                if (raw) mx *= sc;
+                tmem_st32(p_addr, w);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(p_bar[half]);
             }
-            if (my_abort) {
-                any_abort = true;
-                break;
-            }
-            if (band && p.vec_bias) ++nb;
-            // Publish this half's maximum.  The partner's is needed only to
-            // confirm the reference maximum (or, before the first visible
-            // key, to set it), so the exponentials start from the current
-            // reference and are redone in the rare case that it moves.
-            const int xb = jj & 1;
-            sXch[(xb * 2 + half) * 128 + r] = mx;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->x_full[xb]);
-            auto row_max = [&]() -> float {
-                if (!mbar_wait(&bars->x_full[xb], (uint32_t)((jj >> 1) & 1), p.timeout_ns, kSitePrefillXchg, p.err))
-                    bars->abort = 1;
-                return fmaxf(mx, sXch[(xb * 2 + (half ^ 1)) * 128 + r]);
-            };
-            const float c1 = raw ? sl2 : kLog2e;
-            uint32_t w[32];
-            float rsum = 0.f;
-            // This half of P_j (bf16 pairs) and its row sum against the
-            // integer reference m (log2 units): 2^(q(s * c1) - m), with the
-            // score quantised on a fixed grid so that the subtraction is exact.
-            auto exp_pass = [&](float m) {
-                const float offs = kQuantC + (m == -CUDART_INF_F ? 0.f : m);
-                const float2 c12 = make_float2(c1, c1), qc = make_float2(kQuantC, kQuantC),
-                             noff = make_float2(-offs, -offs);
-                float2 rs[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) rs[i] = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float2 x = __fadd2_rn(__ffma2_rn(s[e], c12, qc), noff);
-                    const float2 pe = make_float2(ex2(x.x), ex2(x.y));
-                    rs[e & 3] = __fadd2_rn(rs[e & 3], pe);
-                    w[e] = pack_bf16(pe.x, pe.y);
-                }
-                const float2 rs2 = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
-                rsum = rs2.x + rs2.y;
-            };
-            // Lazy rescaling: the reference maximum m_run (an integer in log2
-            // units) only moves when the row maximum exceeds it by more than
-            // 8, so P stays below 2^8 and O is rescaled rarely (by an exact
-            // power of two); O / l is unchanged.
-            float m_use = m_run;
-            bool grow = false;
-            if (m_run == -CUDART_INF_F) {
-                m_use = ref_max(row_max() * kLog2e);
-                exp_pass(m_use);
-            } else {
-                exp_pass(m_run);
-                const float rmx = row_max() * kLog2e;
-                if (rmx > m_run + kLazyRescale) {
-                    grow = true;
-                    m_use = ref_max(rmx);
-                    exp_pass(m_use);
-                }
-            }
-            const float alpha = grow ? exp2_int(m_run - m_use) : 1.f;
-            // This half of P_j over the S columns this thread has already read
-            // (PV_{j-2}, the last reader of the buffer, completed before S_j).
-            tmem_st32(lane_base + sb * C::BN + kh, w);
-            l_half = l_half * alpha + rsum;
-            m_run = m_use;
 
-            // Rescale this half of the O row when the reference maximum moved
-            // (warp-collective TMEM access): PV_{j-1} must have completed.
-            if (jj >= 1 && __any_sync(0xffffffffu, grow)) {
-                if (!mbar_wait(&bars->o_done[(jj - 1) & 1], (uint32_t)(((jj - 1) >> 1) & 1), p.timeout_ns,
-                               kSitePrefillOFull, p.err))
-                    bars->abort = 1;
-                tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < C::D / 64; ++c) {
-                    uint32_t v[32];
-                    const uint32_t ta = lane_base + C::kOCol + half * (C::D / 2) + c * 32;
-                    tmem_ld32(ta, v);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                    tmem_st32(ta, v);
-                }
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_remote(p_bar[sb]);
-        }
-
-        // Epilogue: O / l, with l the sum of the two halves' partial sums.
-        // (buffer 2: the partner may still read buffer (n_it - 1) % 2 of the last tile)
-        sXch[(4 + half) * 128 + r] = l_half;
-        const bool failed = bar_or(1, 256, any_abort || aborted(bars));
-        const float l_tot = sXch[4 * 128 + r] + sXch[5 * 128 + r];
-        const bool have = n_it > 0 && !failed;
-        if (have) {
-            if (!mbar_wait(&bars->o_final, 0, p.timeout_ns, kSitePrefillOFull, p.err)) bars->abort = 1;
-            tc_fence_after();
-        }
-        const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
-        const bool partial = p.num_splits > 1;
-#pragma unroll
-        for (int c = 0; c < C::D / 64; ++c) {
-            const int col = half * (C::D / 2) + c * 32;  // output dims [col, col + 32)
-            uint32_t v[32];
+            // Epilogue: merge the halves, O = (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / l,
+            // m = max(m_0, m_1), l the same combination of the sums (exact
+            // powers of two); thread (row, half) writes dims [64 half, 64 half + 64).
+            sXch[half * 128 + r] = m_run;
+            sXch[(2 + half) * 128 + r] = l_half;
+            const bool failed = bar_or(1, 256, any_abort || aborted(bars));
+            const float m0 = sXch[r], m1 = sXch[128 + r];
+            const float m_row = fmaxf(m0, m1);
+            const float f0 = m0 == -CUDART_INF_F ? 0.f : exp2_int(m0 - m_row);
+            const float f1 = m1 == -CUDART_INF_F ? 0.f : exp2_int(m1 - m_row);
+            const float l_tot = sXch[2 * 128 + r] * f0 + sXch[3 * 128 + r] * f1;
+            const bool have = n_it > 0 && !failed;
             if (have) {
-                tmem_ld32(lane_base + C::kOCol + col, v);
-                tmem_wait_ld();
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] = 0u;
+                if (!mbar_wait(&bars->o_final, 0, p.timeout_ns, kSitePrefillOFull, p.err)) bars->abort = 1;
+                tc_fence_after();
             }
-            if (!valid) continue;
-            float o[32];
+            const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
+            const float g0 = f0 * inv_l, g1 = f1 * inv_l;
+            const bool partial = p.num_splits > 1;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(v[e]) * inv_l;
-            if (partial) {
-                float* dst = p.ws_o + (((size_t)split * p.T + t) * p.H + h) * C::D + col;
+            for (int c = 0; c < 2; ++c) {
+                const int col = half * 64 + c * 32;  // output dims [col, col + 32)
+                uint32_t v[32], u[32];
+                if (have) {
+                    tmem_ld32(lane_base + C::kOCol + col, v);
+                    tmem_ld32(lane_base + C::kOCol + 128 + col, u);
+                    tmem_wait_ld();
+                } else {
 #pragma unroll
-                for (int e = 0; e < 32; e += 4)
-                    *reinterpret_cast<float4*>(dst + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
-            } else if (p.out_f32) {
-                float* dst = reinterpret_cast<float*>(p.out) + (size_t)t * p.o_st + (size_t)h * p.o_sh + col;
+                    for (int e = 0; e < 32; ++e) v[e] = u[e] = 0u;
+                }
+                if (!valid) continue;
+                float o[32];
 #pragma unroll
-                for (int e = 0; e < 32; e += 4)
-                    *reinterpret_cast<float4*>(dst + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
-            } else {
-                uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + (size_t)t * p.o_st + (size_t)h * p.o_sh + col;
+                for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(v[e]) * g0 + __uint_as_float(u[e]) * g1;
+                if (partial) {
+                    float* dst = p.ws_o + (((size_t)split * p.T + t) * p.H + h) * C::D + col;
 #pragma unroll
-                for (int e = 0; e < 32; e += 8) {
-                    uint4 pk;
-                    pk.x = pack_bf16(o[e], o[e + 1]);
-                    pk.y = pack_bf16(o[e + 2], o[e + 3]);
-                    pk.z = pack_bf16(o[e + 4], o[e + 5]);
-                    pk.w = pack_bf16(o[e + 6], o[e + 7]);
-                    *reinterpret_cast<uint4*>(dst + e) = pk;
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4*>(dst + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                } else if (p.out_f32) {
+                    float* dst = reinterpret_cast<float*>(p.out) + (size_t)t * p.o_st + (size_t)h * p.o_sh + col;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4*>(dst + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                } else {
+                    uint16_t* dst =
+                        reinterpret_cast<uint16_t*>(p.out) + (size_t)t * p.o_st + (size_t)h * p.o_sh + col;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 pk;
+                        pk.x = pack_bf16(o[e], o[e + 1]);
+                        pk.y = pack_bf16(o[e + 2], o[e + 3]);
+                        pk.z = pack_bf16(o[e + 4], o[e + 5]);
+                        pk.w = pack_bf16(o[e + 6], o[e + 7]);
+                        *reinterpret_cast<uint4*>(dst + e) = pk;
+                    }
                 }
             }
+            if (valid && partial && half == 0)
+                p.ws_lse[((size_t)split * p.T + t) * p.H + h] = l_tot > 0.f ? m_row + __log2f(l_tot) : -CUDART_INF_F;
+            if (valid && !partial && half == 0 && p.lse)
+                p.lse[(size_t)t * p.lse_st + (size_t)h * p.lse_sh] =
+                    l_tot > 0.f ? (m_row + __log2f(l_tot)) * kLn2 : -CUDART_INF_F;
+        } else {
+
+            for (int jj = 0; jj < n_it; ++jj) {
+                const int sb = jj & 1;
+                const int j0 = key_block(jj) * C::BN;
+                const int jh = j0 + kh;  // first key of this half
+                const bool band = band_tile(j0);
+                bool my_abort = !mbar_wait(&bars->s_full[sb], (uint32_t)((jj >> 1) & 1), p.timeout_ns, kSitePrefillSFull,
+                                           p.err);
+                my_abort = __any_sync(0xffffffffu, my_abort || aborted(bars));
+                float2 s[32];  // keys (kh + 2e, kh + 2e + 1) of the tile
+                float mx = -CUDART_INF_F;
+                // raw: s keeps q.k (no bias on this tile); the scale folds into
+                // the exponent.  Otherwise s holds sc * q.k + bias.
+                const bool raw = !band && pos_scale;
+                if (!my_abort) {
+                    tc_fence_after();
+                    {
+                        uint32_t v0[32], v1[32];
+                        tmem_ld32(lane_base + sb * C::BN + kh, v0);
+                        tmem_ld32(lane_base + sb * C::BN + kh + 32, v1);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            s[e] = make_float2(__uint_as_float(v0[2 * e]), __uint_as_float(v0[2 * e + 1]));
+                            s[16 + e] = make_float2(__uint_as_float(v1[2 * e]), __uint_as_float(v1[2 * e + 1]));
+                        }
+                    }
+                    tc_fence_before();
+                    if (!raw) {
+                        const float2 sc2 = make_float2(sc, sc);
+                        if (band && p.vec_bias) {
+                            const int bb = nb % C::kBiasBufs;
+                            if (!mbar_wait(&bars->bias_full[bb], (uint32_t)((nb / C::kBiasBufs) & 1), p.timeout_ns,
+                                           kSitePrefillRelFull, p.err))
+                                bars->abort = 1;
+                            const uint32_t* wb = wrow + bb * (C::kBiasBytes / 4);
+                            uint32_t wv[33];
+#pragma unroll
+                            for (int i = 0; i < 33; ++i) wv[i] = wb[i];
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) {
+                                const uint32_t pr = __byte_perm(wv[31 - e], wv[32 - e], psel);
+                                s[e] = __ffma2_rn(s[e], sc2,
+                                                  make_float2(__uint_as_float(pr & 0xffff0000u), __uint_as_float(pr << 16)));
+                            }
+                            // Every read of this band tile's windows is done.
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&bars->bias_empty[bb]);
+                        } else if (band) {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) {
+                                const int d = pos - (jh + 2 * e);
+                                const float b0 = valid && d >= 0 && d < R ? rel_at(p.rel, bias_f32, rel_row + d) : 0.f;
+                                const float b1 =
+                                    valid && d - 1 >= 0 && d - 1 < R ? rel_at(p.rel, bias_f32, rel_row + d - 1) : 0.f;
+                                s[e] = __ffma2_rn(s[e], sc2, make_float2(b0, b1));
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) s[e] = __fmul2_rn(s[e], sc2);
+                        }
+                    }
+                    // Mask (warp-uniform skip when every row of the warp sees the whole half tile).
+                    const bool row_full = !valid || (jh >= klo && jh + 64 <= khi);
+                    if (!__all_sync(0xffffffffu, row_full)) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const int j = jh + 2 * e;
+                            if (!row_full && !(j >= klo && j < khi)) s[e].x = -CUDART_INF_F;
+                            if (!row_full && !(j + 1 >= klo && j + 1 < khi)) s[e].y = -CUDART_INF_F;
+                        }
+                    }
+                    float mk[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mk[i] = fmax3(s[i].x, s[i].y, s[8 + i].x);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mk[i] = fmax3(mk[i], s[8 + i].y, s[16 + i].x);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mk[i] = fmax3(mk[i], s[16 + i].y, s[24 + i].x);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mk[i] = fmaxf(mk[i], s[24 + i].y);
+                    mx = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]), fmaxf(mk[6], mk[7]));
+                    if (raw) mx *= sc;
+                }
+                if (my_abort) {
+                    any_abort = true;
+                    break;
+                }
+                if (band && p.vec_bias) ++nb;
+                // Publish this half's maximum.  The partner's is needed only to
+                // confirm the reference maximum (or, before the first visible
+                // key, to set it), so the exponentials start from the current
+                // reference and are redone in the rare case that it moves.
+                const int xb = jj & 1;
+                sXch[(xb * 2 + half) * 128 + r] = mx;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->x_full[xb]);
+                auto row_max = [&]() -> float {
+                    if (!mbar_wait(&bars->x_full[xb], (uint32_t)((jj >> 1) & 1), p.timeout_ns, kSitePrefillXchg, p.err))
+                        bars->abort = 1;
+                    return fmaxf(mx, sXch[(xb * 2 + (half ^ 1)) * 128 + r]);
+                };
+                const float c1 = raw ? sl2 : kLog2e;
+                uint32_t w[32];
+                float rsum = 0.f;
+                // This half of P_j (bf16 pairs) and its row sum against the
+                // integer reference m (log2 units): 2^(q(s * c1) - m), with the
+                // score quantised on a fixed grid so that the subtraction is exact.
+                auto exp_pass = [&](float m) {
+                    const float offs = kQuantC + (m == -CUDART_INF_F ? 0.f : m);
+                    const float2 c12 = make_float2(c1, c1), qc = make_float2(kQuantC, kQuantC),
+                                 noff = make_float2(-offs, -offs);
+                    float2 rs[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) rs[i] = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float2 x = __fadd2_rn(__ffma2_rn(s[e], c12, qc), noff);
+                        const float2 pe = make_float2(ex2(x.x), ex2(x.y));
+                        rs[e & 3] = __fadd2_rn(rs[e & 3], pe);
+                        w[e] = pack_bf16(pe.x, pe.y);
+                    }
+                    const float2 rs2 = __fadd2_rn(__fadd2_rn(rs[0], rs[1]), __fadd2_rn(rs[2], rs[3]));
+                    rsum = rs2.x + rs2.y;
+                };
+                // Lazy rescaling: the reference maximum m_run (an integer in log2
+                // units) only moves when the row maximum exceeds it by more than
+                // 8, so P stays below 2^8 and O is rescaled rarely (by an exact
+                // power of two); O / l is unchanged.
+                float m_use = m_run;
+                bool grow = false;
+                if (m_run == -CUDART_INF_F) {
+                    m_use = ref_max(row_max() * kLog2e);
+                    exp_pass(m_use);
+                } else {
+                    exp_pass(m_run);
+                    const float rmx = row_max() * kLog2e;
+                    if (rmx > m_run + kLazyRescale) {
+                        grow = true;
+                        m_use = ref_max(rmx);
+                        exp_pass(m_use);
+                    }
+                }
+                const float alpha = grow ? exp2_int(m_run - m_use) : 1.f;
+                // This half of P_j over the S columns this thread has already read
+                // (PV_{j-2}, the last reader of the buffer, completed before S_j).
+                tmem_st32(lane_base + sb * C::BN + kh, w);
+                l_half = l_half * alpha + rsum;
+                m_run = m_use;
+
+                // Rescale this half of the O row when the reference maximum moved
+                // (warp-collective TMEM access): PV_{j-1} must have completed.
+                if (jj >= 1 && __any_sync(0xffffffffu, grow)) {
+                    if (!mbar_wait(&bars->o_done[(jj - 1) & 1], (uint32_t)(((jj - 1) >> 1) & 1), p.timeout_ns,
+                                   kSitePrefillOFull, p.err))
+                        bars->abort = 1;
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < C::D / 64; ++c) {
+                        uint32_t v[32];
+                        const uint32_t ta = lane_base + C::kOCol + half * (C::D / 2) + c * 32;
+                        tmem_ld32(ta, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                        tmem_st32(ta, v);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(p_bar[sb]);
+            }
+
+            // Epilogue: O / l, with l the sum of the two halves' partial sums.
+            // (buffer 2: the partner may still read buffer (n_it - 1) % 2 of the last tile)
+            sXch[(4 + half) * 128 + r] = l_half;
+            const bool failed = bar_or(1, 256, any_abort || aborted(bars));
+            const float l_tot = sXch[4 * 128 + r] + sXch[5 * 128 + r];
+            const bool have = n_it > 0 && !failed;
+            if (have) {
+                if (!mbar_wait(&bars->o_final, 0, p.timeout_ns, kSitePrefillOFull, p.err)) bars->abort = 1;
+                tc_fence_after();
+            }
+            const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
+            const bool partial = p.num_splits > 1;
+#pragma unroll
+            for (int c = 0; c < C::D / 64; ++c) {
+                const int col = half * (C::D / 2) + c * 32;  // output dims [col, col + 32)
+                uint32_t v[32];
+                if (have) {
+                    tmem_ld32(lane_base + C::kOCol + col, v);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = 0u;
+                }
+                if (!valid) continue;
+                float o[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(v[e]) * inv_l;
+                if (partial) {
+                    float* dst = p.ws_o + (((size_t)split * p.T + t) * p.H + h) * C::D + col;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4*>(dst + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                } else if (p.out_f32) {
+                    float* dst = reinterpret_cast<float*>(p.out) + (size_t)t * p.o_st + (size_t)h * p.o_sh + col;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4*>(dst + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                } else {
+                    uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + (size_t)t * p.o_st + (size_t)h * p.o_sh + col;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 pk;
+                        pk.x = pack_bf16(o[e], o[e + 1]);
+                        pk.y = pack_bf16(o[e + 2], o[e + 3]);
+                        pk.z = pack_bf16(o[e + 4], o[e + 5]);
+                        pk.w = pack_bf16(o[e + 6], o[e + 7]);
+                        *reinterpret_cast<uint4*>(dst + e) = pk;
+                    }
+                }
+            }
+            if (valid && partial && half == 0)
+                p.ws_lse[((size_t)split * p.T + t) * p.H + h] = l_tot > 0.f ? m_run + __log2f(l_tot) : -CUDART_INF_F;
+            if (valid && !partial && half == 0 && p.lse)
+                p.lse[(size_t)t * p.lse_st + (size_t)h * p.lse_sh] =
+                    l_tot > 0.f ? (m_run + __log2f(l_tot)) * kLn2 : -CUDART_INF_F;
         }
-        if (valid && partial && half == 0)
-            p.ws_lse[((size_t)split * p.T + t) * p.H + h] = l_tot > 0.f ? m_run + __log2f(l_tot) : -CUDART_INF_F;
-        if (valid && !partial && half == 0 && p.lse)
-            p.lse[(size_t)t * p.lse_st + (size_t)h * p.lse_sh] =
-                l_tot > 0.f ? (m_run + __log2f(l_tot)) * kLn2 : -CUDART_INF_F;
     }
 
     // Both CTAs are done with TMEM and with each other's barriers.
